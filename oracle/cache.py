@@ -1,0 +1,229 @@
+"""The oracle's KV cache: append log, residency, attend, masses, scores, selection.
+
+Test infrastructure only (see the package docstring).
+
+What one decode step computes (per layer l and sequence b, then per step):
+  a1  append: the new token's K and V are stored (FP8: codes + one scale per position
+      per cache, ``oracle.e4m3``), at absolute position p = next_position[l][b];
+      next_position advances by the number of new tokens.
+      ("Context Optimization", FP8 KV Cache > How It Works and Sliding Window
+      Attention > Design; "LLM mechanics III", sections 1 and 5.)
+  a2  attend: the query of every head attends over the resident entries.
+      Window W: position p is resident while p >= next_position - W (the current
+      token included, "LLM mechanics III" section 1).  H2O: every entry of a
+      resident 16-token block ("Context Optimization", H2O).  No window: all.
+  a3  masses: token mass = sum over query heads of the weights; block mass = max over
+      query heads of the in-block weight sum ("Per-Head Attention as a Scoring
+      Signal", Fix: score per head, place per block).
+  a4  accumulate (once per step, after every layer): token score x_p = sum over
+      layers of the token masses; block score y_k = max over layers of the block
+      masses; cumulative C += x and EMA E = d*E + (1-d)*x for every tracked entry
+      (every position < next_position, every block holding one), x = 0 where nothing
+      attended ("Context views at marginal cost", Tier 1: EMA + Cumulative kept as
+      O(1)-per-entry running reductions; "Context Optimization", H2O step 1).
+  a5  select: top-k resident blocks by C (or E) with ties to the lower block id;
+      with H2O the sink and recent blocks are protected and eviction may be applied.
+
+Where the pages leave a step open, the module docstrings of ``attention``,
+``selection`` and ``e4m3`` state the reading taken.
+Everything is float64 and written out plainly; no blocking or reordering.
+"""
+
+import numpy as np
+
+from . import attention, e4m3, selection
+
+
+class ScoreTables:
+    """Cumulative and EMA tables of one sequence, per token and per block."""
+
+    def __init__(self, max_positions, block_tokens=16, ema_decay=0.9):
+        self.block_tokens = block_tokens
+        self.d = float(ema_decay)
+        nb = -(-max_positions // block_tokens)
+        self.c_tok = np.zeros(max_positions)
+        self.e_tok = np.zeros(max_positions)
+        self.c_blk = np.zeros(nb)
+        self.e_blk = np.zeros(nb)
+        self.steps = 0
+
+    def update(self, tracked_positions, x_tok, y_blk):
+        """One step.  x_tok: float64 array over positions 0..tracked_positions-1 with
+        the step's token scores (0 where nothing attended); y_blk: float64 array over
+        the blocks holding a tracked position, likewise.  Every tracked entry is
+        updated: C += x, E = d*E + (1-d)*x."""
+        d = self.d
+        n = tracked_positions
+        nb = -(-n // self.block_tokens)
+        x = np.asarray(x_tok, np.float64)
+        y = np.asarray(y_blk, np.float64)
+        if x.shape != (n,) or y.shape != (nb,):
+            raise ValueError("score arrays must cover exactly the tracked entries")
+        self.c_tok[:n] = self.c_tok[:n] + x
+        self.e_tok[:n] = d * self.e_tok[:n] + (1.0 - d) * x
+        self.c_blk[:nb] = self.c_blk[:nb] + y
+        self.e_blk[:nb] = d * self.e_blk[:nb] + (1.0 - d) * y
+        self.steps += 1
+
+
+class OracleKV:
+    """Float64 model of the whole path for ``num_seqs`` sequences."""
+
+    def __init__(self, *, num_layers, num_q_heads, num_kv_heads, head_dim, num_seqs,
+                 max_positions, kv_format="bf16", window=0, h2o_budget_tokens=0,
+                 h2o_sink_tokens=4, h2o_recent_frac=0.25, ema_decay=0.9, block_tokens=16):
+        if num_q_heads % num_kv_heads:
+            raise ValueError("num_q_heads must be a multiple of num_kv_heads")
+        if window < 0:
+            raise ValueError("window must be >= 0 (0 = none)")
+        if kv_format not in ("f32", "bf16", "e4m3"):
+            raise ValueError("kv_format")
+        self.L, self.Hq, self.Hkv, self.D = num_layers, num_q_heads, num_kv_heads, head_dim
+        self.B, self.P = num_seqs, max_positions
+        self.fmt = kv_format
+        self.block = block_tokens
+        # H2O takes priority over the window when both are set
+        # ("Context Optimization", H2O vs Sliding Window).
+        if h2o_budget_tokens > 0:
+            self.mode = "h2o"
+            self.window = 0
+        elif window > 0:
+            self.mode = "window"
+            self.window = window
+        else:
+            self.mode = "none"
+            self.window = 0
+        self.h2o_budget_tokens = h2o_budget_tokens
+        self.h2o_budget_blocks = h2o_budget_tokens // block_tokens
+        self.h2o_sink_tokens = h2o_sink_tokens
+        self.h2o_recent_tokens = selection.recent_token_count(h2o_budget_tokens, h2o_recent_frac)
+        self.next_position = np.zeros((num_layers, num_seqs), dtype=np.int64)
+        shape = (num_layers, num_seqs, max_positions, num_kv_heads, head_dim)
+        if kv_format == "e4m3":
+            self.k_codes = np.zeros(shape, dtype=np.uint8)
+            self.v_codes = np.zeros(shape, dtype=np.uint8)
+            self.k_scale = np.zeros(shape[:3])
+            self.v_scale = np.zeros(shape[:3])
+        else:
+            # bf16 and f32 inputs are binary32 numbers: float32 storage is exact
+            self.k_vals = np.zeros(shape, dtype=np.float32)
+            self.v_vals = np.zeros(shape, dtype=np.float32)
+        self.resident_blocks = [set() for _ in range(num_seqs)]      # H2O mode only
+        self.scores = [ScoreTables(max_positions, block_tokens, ema_decay) for _ in range(num_seqs)]
+        self._tok_mass = {}      # (l, b) -> (positions, token mass) of the current step
+        self._blk_mass = {}      # (l, b) -> {block: mass} of the current step
+
+    # ---------------------------------------------------------------- a1 append
+    def append(self, layer, seq, k, v):
+        """k, v: [n_new, Hkv, D] exact input values.  Returns the absolute positions."""
+        k = np.asarray(k, np.float64)
+        v = np.asarray(v, np.float64)
+        n = k.shape[0]
+        past = int(self.next_position[layer, seq])
+        if past + n > self.P:
+            raise ValueError("position capacity exceeded")
+        pos = np.arange(past, past + n)
+        if self.fmt == "e4m3":
+            kc, ks = e4m3.quantise_positions(k)
+            vc, vs = e4m3.quantise_positions(v)
+            self.k_codes[layer, seq, pos] = kc
+            self.v_codes[layer, seq, pos] = vc
+            self.k_scale[layer, seq, pos] = ks
+            self.v_scale[layer, seq, pos] = vs
+        else:
+            self.k_vals[layer, seq, pos] = k
+            self.v_vals[layer, seq, pos] = v
+        if self.mode == "h2o":
+            for p in pos:
+                self.resident_blocks[seq].add(int(p) // self.block)
+        self.next_position[layer, seq] = past + n
+        return pos
+
+    def slot_of(self, position):
+        """Storage slot of an absolute position (window: p % W; otherwise p)."""
+        return position % self.window if self.mode == "window" else position
+
+    # ---------------------------------------------------------------- residency
+    def resident_positions(self, layer, seq):
+        nxt = int(self.next_position[layer, seq])
+        if self.mode == "window":
+            return np.arange(max(0, nxt - self.window), nxt)
+        if self.mode == "h2o":
+            p = np.arange(nxt)
+            keep = np.isin(p // self.block, np.array(sorted(self.resident_blocks[seq]), np.int64))
+            return p[keep]
+        return np.arange(nxt)
+
+    def resident_block_ids(self, seq, layer=0):
+        pos = self.resident_positions(layer, seq)
+        return sorted(set(int(p) // self.block for p in pos))
+
+    def stored_kv(self, layer, seq, positions):
+        """Dequantised float64 K, V of the given positions: [n, Hkv, D] each."""
+        if self.fmt == "e4m3":
+            k = e4m3.dequantise(self.k_codes[layer, seq, positions], self.k_scale[layer, seq, positions])
+            v = e4m3.dequantise(self.v_codes[layer, seq, positions], self.v_scale[layer, seq, positions])
+            return k, v
+        return (self.k_vals[layer, seq, positions].astype(np.float64),
+                self.v_vals[layer, seq, positions].astype(np.float64))
+
+    # ---------------------------------------------------------------- a2/a3 attend
+    def attend(self, layer, seq, q):
+        """q: [Hq, D].  Returns (out [Hq, D], weights [Hq, n], positions [n])."""
+        pos = self.resident_positions(layer, seq)
+        k, v = self.stored_kv(layer, seq, pos)
+        out, w = attention.decode_attention(q, k, v)
+        self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(w))
+        self._blk_mass[(layer, seq)] = attention.block_step_mass(w, pos, self.block)
+        return out, w, pos
+
+    def token_mass(self, layer, seq):
+        """(positions, token mass) of the last attend of (layer, seq)."""
+        return self._tok_mass[(layer, seq)]
+
+    def block_mass(self, layer, seq):
+        """{block: mass} of the last attend of (layer, seq)."""
+        return self._blk_mass[(layer, seq)]
+
+    # ---------------------------------------------------------------- a4 accumulate
+    def accumulate(self, seqs=None):
+        """Fold the masses of every layer into the score tables.  Returns per sequence
+        the step's (x_tok, y_blk) arrays over the tracked positions / blocks."""
+        seqs = range(self.B) if seqs is None else seqs
+        result = {}
+        for b in seqs:
+            nxt = set(int(self.next_position[l, b]) for l in range(self.L))
+            if len(nxt) != 1:
+                raise ValueError("layers disagree on next_position at accumulate")
+            n = nxt.pop()
+            x_tok = np.zeros(n)
+            y_blk = np.zeros(-(-n // self.block))
+            for l in range(self.L):
+                if (l, b) not in self._tok_mass:
+                    raise ValueError("layer %d of sequence %d was not attended this step" % (l, b))
+                pos, tau = self._tok_mass.pop((l, b))
+                x_tok[pos] += tau                      # sum over layers
+                for k, m in self._blk_mass.pop((l, b)).items():
+                    y_blk[k] = max(y_blk[k], m)        # max over layers
+            self.scores[b].update(n, x_tok, y_blk)
+            result[b] = (x_tok, y_blk)
+        return result
+
+    # ---------------------------------------------------------------- a5 select
+    def select(self, seq, k, score_kind="cumulative", protect=False, apply=False):
+        """Kept block ids (ascending).  protect: H2O sink/recent protection with k as
+        the block budget; apply: evict the unkept blocks (H2O mode only)."""
+        cand = self.resident_block_ids(seq)
+        table = self.scores[seq].c_blk if score_kind == "cumulative" else self.scores[seq].e_blk
+        scores = {c: table[c] for c in cand}
+        nxt = int(self.next_position[0, seq])
+        if protect:
+            keep = selection.h2o_keep(cand, scores, k, nxt, self.h2o_sink_tokens,
+                                      self.h2o_recent_tokens, self.block)
+        else:
+            keep = selection.top_k_blocks(cand, scores, k)
+        if apply:
+            if self.mode != "h2o":
+                raise ValueError("eviction applies to the H2O mode only")
+            self.resident_blocks[seq] = set(keep)
+        return keep
