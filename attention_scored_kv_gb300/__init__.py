@@ -1,0 +1,190 @@
+"""Python binding of libkvs, the attention-scored KV cache decode path for GB300.
+
+Thin marshalling over the C ABI in include/kvs.h: each method takes torch tensors that
+already live on the GPU, checks their dtype / shape / contiguity and passes raw device
+pointers and the current CUDA stream to the library.  Every step of the path (append,
+attend with the fused mass epilogue, accumulate, select) runs in the library's CUDA
+kernels; PyTorch provides device memory and streams only.  If libkvs.so is missing the
+calls raise: there is no CPU or PyTorch fallback.
+"""
+
+import ctypes
+
+import torch
+
+from . import _abi
+from ._abi import (  # noqa: F401
+    F32, BF16, E4M3, SCORE_CUMULATIVE, SCORE_EMA, KERNEL_AUTO, KERNEL_GENERAL, KERNEL_TENSOR,
+    MODE_NONE, MODE_WINDOW, MODE_H2O, SELECT_PROTECT, SELECT_APPLY, Config, Layout,
+)
+from ._abi import (  # noqa: F401
+    STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
+    STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
+    STATE_BLOCK_TABLE,
+)
+
+_TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+class KVSError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__("%s: %s" % (_abi.STATUS_NAMES.get(status, status), message))
+
+
+def lib():
+    return _abi.load()
+
+
+def config_init(**fields):
+    """A kvs_config with the library defaults, then the given fields."""
+    cfg = Config()
+    lib().kvs_config_init(ctypes.byref(cfg))
+    for k, v in fields.items():
+        setattr(cfg, k, v)
+    return cfg
+
+
+def validate_config(cfg):
+    """(status, message) of the host-side config check."""
+    buf = ctypes.create_string_buffer(512)
+    st = lib().kvs_validate_config(ctypes.byref(cfg), buf, len(buf))
+    return st, buf.value.decode()
+
+
+def workspace_bytes(cfg):
+    return int(lib().kvs_workspace_bytes(ctypes.byref(cfg)))
+
+
+def status_string(status):
+    return lib().kvs_status_string(status).decode()
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s, got %s" % (name, tuple(shape), tuple(t.shape)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+class KVCache:
+    """A kvs context bound to a workspace this object owns (a torch uint8 tensor)."""
+
+    def __init__(self, cfg, device=None, stream=None):
+        st, msg = validate_config(cfg)
+        if st != _abi.OK:
+            raise KVSError(st, msg)
+        self.cfg = cfg
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        nbytes = workspace_bytes(cfg)
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        self._ctx = ctypes.c_void_p()
+        with torch.cuda.device(self.device):
+            st = lib().kvs_create(ctypes.byref(cfg), _ptr(self.workspace), nbytes, _stream(stream),
+                                  ctypes.byref(self._ctx))
+        if st != _abi.OK:
+            raise KVSError(st, "kvs_create failed")
+        self.in_dtype = _TORCH_DT[cfg.in_dtype]
+        L, Hq, Hkv, D = cfg.num_layers, cfg.num_q_heads, cfg.num_kv_heads, cfg.head_dim
+        self.shape = (L, Hq, Hkv, D)
+
+    def __del__(self):
+        if getattr(self, "_ctx", None) and self._ctx.value:
+            try:
+                lib().kvs_destroy(self._ctx)
+            except Exception:
+                pass
+            self._ctx = None
+
+    def _check(self, st):
+        if st != _abi.OK:
+            raise KVSError(st, lib().kvs_last_error(self._ctx).decode())
+
+    # ---- the path
+    def reset(self, seq_begin=0, n_seqs=None, stream=None):
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        self._check(lib().kvs_reset(self._ctx, seq_begin, n, _stream(stream)))
+
+    def append_kv(self, layer, k, v, seq_begin=0, stream=None):
+        """k, v: [n_seqs, n_new, Hkv, D] in the input dtype."""
+        _, _, Hkv, D = self.shape
+        n_seqs, n_new = int(k.shape[0]), int(k.shape[1])
+        _need(k, "k", self.in_dtype, (n_seqs, n_new, Hkv, D))
+        _need(v, "v", self.in_dtype, (n_seqs, n_new, Hkv, D))
+        self._check(lib().kvs_append_kv(self._ctx, layer, seq_begin, n_seqs, n_new, _ptr(k), _ptr(v),
+                                        _stream(stream)))
+
+    def decode_attend(self, layer, q, out=None, seq_begin=0, stream=None):
+        """q: [n_seqs, Hq, D] in the input dtype; returns out [n_seqs, Hq, D] float32."""
+        _, Hq, _, D = self.shape
+        n_seqs = int(q.shape[0])
+        _need(q, "q", self.in_dtype, (n_seqs, Hq, D))
+        if out is None:
+            out = torch.empty((n_seqs, Hq, D), dtype=torch.float32, device=q.device)
+        _need(out, "out", torch.float32, (n_seqs, Hq, D))
+        self._check(lib().kvs_decode_attend(self._ctx, layer, seq_begin, n_seqs, _ptr(q), _ptr(out),
+                                            _stream(stream)))
+        return out
+
+    def accumulate_scores(self, seq_begin=0, n_seqs=None, stream=None):
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        self._check(lib().kvs_accumulate_scores(self._ctx, seq_begin, n, _stream(stream)))
+
+    def select_blocks(self, k, seq_begin=0, n_seqs=None, score_kind=SCORE_CUMULATIVE, flags=0, keep_capacity=None,
+                      keep_ids=None, keep_count=None, stream=None):
+        """k: an int (same for every sequence) or an int32 CUDA tensor [n_seqs].
+        Returns (keep_ids [n_seqs, keep_capacity] int32, keep_count [n_seqs] int32)."""
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        cap = self.layout().max_blocks if keep_capacity is None else keep_capacity
+        if keep_ids is None:
+            keep_ids = torch.full((n, cap), -1, dtype=torch.int32, device=self.device)
+        if keep_count is None:
+            keep_count = torch.zeros(n, dtype=torch.int32, device=self.device)
+        _need(keep_ids, "keep_ids", torch.int32, (n, cap))
+        _need(keep_count, "keep_count", torch.int32, (n,))
+        if isinstance(k, torch.Tensor):
+            _need(k, "k", torch.int32, (n,))
+            kp, ku = _ptr(k), 0
+        else:
+            kp, ku = None, int(k)
+        self._check(lib().kvs_select_blocks(self._ctx, seq_begin, n, kp, ku, score_kind, flags, _ptr(keep_ids),
+                                            cap, _ptr(keep_count), _stream(stream)))
+        return keep_ids, keep_count
+
+    # ---- inspection
+    def read_state(self, what, layer=0, stream=None):
+        """A raw copy (uint8 CUDA tensor) of one state array; see kvs_state_item."""
+        n = int(lib().kvs_state_bytes(self._ctx, what))
+        if n == 0:
+            raise KVSError(_abi.ERR_INVALID_ARGUMENT, "state item %d not available" % what)
+        dst = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self._check(lib().kvs_read_state(self._ctx, what, layer, _ptr(dst), n, _stream(stream)))
+        return dst
+
+    def layout(self):
+        lay = Layout()
+        self._check(lib().kvs_get_layout(self._ctx, ctypes.byref(lay)))
+        return lay
+
+    def get_status(self, stream=None):
+        """Synchronise and return the device status code (0 = OK)."""
+        return lib().kvs_get_status(self._ctx, _stream(stream))
+
+    def clear_error(self, stream=None):
+        self._check(lib().kvs_clear_error(self._ctx, _stream(stream)))
+
+    def last_error(self):
+        return lib().kvs_last_error(self._ctx).decode()

@@ -1,0 +1,552 @@
+// The C ABI of libkvs: argument checks, workspace plan, host shadows, dispatch.
+//
+// Host shadows: the context keeps next_position per (layer, sequence), the allocation
+// frontier and (H2O) a bound on resident blocks per sequence, so every call can be
+// checked and sized without reading device memory.  The device holds the truth; a
+// replayed CUDA graph advances the device state but not these shadows.
+#include <cuda.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "kvs_internal.cuh"
+
+namespace kvs {
+bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window, int mode);
+cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
+cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
+                             int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound, int grid,
+                             cudaStream_t st);
+int tc_grid(int kv_dtype, int Hkv, int sm_count);
+}  // namespace kvs
+
+using namespace kvs;
+
+namespace {
+
+constexpr int32_t kDefaultSpin = 5000000;   // ~0.5 s of 100 ns polls
+
+struct Plan {
+  int mode = 0, pages_per_seq = 0, num_pages = 0, max_blocks = 0, res_blocks_per_seq = 0;
+  int recent_tokens = 0;
+  size_t page_bytes = 0, logit_elems = 0, total = 0;
+  // region offsets
+  size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
+  size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
+  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, steps, acc_tickets;
+  size_t partials, counters, logits, err;
+};
+
+size_t esize(int dt) { return dt == KVS_F32 ? 4 : (dt == KVS_BF16 ? 2 : 1); }
+
+void put(char* msg, size_t n, const char* fmt, ...) {
+  if (!msg || n == 0) return;
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(msg, n, fmt, ap);
+  va_end(ap);
+}
+
+kvs_status check_config(const kvs_config* c, char* msg, size_t n) {
+  if (!c) { put(msg, n, "config is NULL"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->num_layers < 1) { put(msg, n, "num_layers must be >= 1"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->num_q_heads < 1 || c->num_kv_heads < 1 || c->num_q_heads % c->num_kv_heads) {
+    put(msg, n, "num_q_heads must be a positive multiple of num_kv_heads");
+    return KVS_ERR_INVALID_ARGUMENT;
+  }
+  if (c->head_dim != 16 && c->head_dim != 32 && c->head_dim != 64 && c->head_dim != 128) {
+    put(msg, n, "head_dim must be 16, 32, 64 or 128");
+    return KVS_ERR_UNSUPPORTED;
+  }
+  if (c->max_seqs < 1 || c->max_positions < 1) { put(msg, n, "max_seqs and max_positions must be >= 1"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->max_positions > (1 << 30)) { put(msg, n, "max_positions too large"); return KVS_ERR_UNSUPPORTED; }
+  if (c->window < 0) { put(msg, n, "window must be >= 0 (0 = none)"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->block_tokens != kBlock) { put(msg, n, "block_tokens must be 16"); return KVS_ERR_UNSUPPORTED; }
+  if (c->h2o_budget_tokens < 0 || (c->h2o_budget_tokens % kBlock)) {
+    put(msg, n, "h2o_budget_tokens must be 0 or a positive multiple of 16");
+    return KVS_ERR_INVALID_ARGUMENT;
+  }
+  if (c->h2o_sink_tokens < 0) { put(msg, n, "h2o_sink_tokens must be >= 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (!(c->h2o_recent_frac >= 0.0 && c->h2o_recent_frac <= 1.0)) { put(msg, n, "h2o_recent_frac must be in [0, 1]"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (!(c->ema_decay >= 0.0 && c->ema_decay < 1.0)) { put(msg, n, "ema_decay must be in [0, 1)"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->num_pages < 0) { put(msg, n, "num_pages must be >= 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->kernel < 0 || c->kernel > 2) { put(msg, n, "kernel must be a kvs_kernel"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->spin_limit < -1) { put(msg, n, "spin_limit must be >= -1"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->kv_dtype < KVS_F32 || c->kv_dtype > KVS_E4M3) { put(msg, n, "kv_dtype must be F32, BF16 or E4M3"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->in_dtype != KVS_F32 && c->in_dtype != KVS_BF16) { put(msg, n, "in_dtype must be F32 or BF16"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->kv_dtype == KVS_BF16 && c->in_dtype != KVS_BF16) {
+    put(msg, n, "a bf16 cache needs bf16 inputs (f32 would be rounded)");
+    return KVS_ERR_UNSUPPORTED;
+  }
+  for (int i = 0; i < 5; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  for (int i = 0; i < 2; ++i) if (c->reserved_d[i] != 0.0) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  const int mode = c->h2o_budget_tokens > 0 ? KVS_MODE_H2O : (c->window > 0 ? KVS_MODE_WINDOW : KVS_MODE_NONE);
+  const bool tc = tc_supported(c->num_q_heads, c->num_kv_heads, c->head_dim, c->kv_dtype, c->in_dtype, c->window, mode);
+  if (c->kernel == KVS_KERNEL_TENSOR && !tc) {
+    put(msg, n, "the tensor-core kernel needs head_dim 128, 8 query heads per KV head (4 or 8 KV heads), bf16 "
+                "inputs, bf16 or E4M3 storage and a window that is 0 or a multiple of 16");
+    return KVS_ERR_UNSUPPORTED;
+  }
+  if (msg && n) msg[0] = 0;
+  return KVS_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+void make_plan(const kvs_config* c, Plan* p) {
+  const size_t L = c->num_layers, B = c->max_seqs, Hq = c->num_q_heads, D = c->head_dim;
+  p->mode = c->h2o_budget_tokens > 0 ? KVS_MODE_H2O : (c->window > 0 ? KVS_MODE_WINDOW : KVS_MODE_NONE);
+  p->max_blocks = (int)cdiv64(c->max_positions, kBlock);
+  if (p->mode == KVS_MODE_WINDOW) {
+    p->pages_per_seq = (int)cdiv64(c->window, kBlock);
+    p->num_pages = (int)(B * p->pages_per_seq);
+    p->res_blocks_per_seq = std::min<int>(p->max_blocks, p->pages_per_seq + 1);
+  } else if (p->mode == KVS_MODE_NONE) {
+    p->pages_per_seq = p->max_blocks;
+    p->num_pages = (int)(B * p->max_blocks);
+    p->res_blocks_per_seq = p->max_blocks;
+  } else {
+    p->pages_per_seq = 0;
+    p->num_pages = c->num_pages > 0 ? c->num_pages : (int)(B * p->max_blocks);
+    p->res_blocks_per_seq = p->max_blocks;
+  }
+  p->recent_tokens = (int)std::ceil(c->h2o_recent_frac * c->h2o_budget_tokens);
+  p->page_bytes = (size_t)c->num_kv_heads * kBlock * D * esize(c->kv_dtype);
+  const size_t NP = p->num_pages, slots = NP * kBlock, MB = p->max_blocks, P = c->max_positions;
+  // logits: the general kernel needs [seq][Hq][entries]; the tensor kernel per-CTA shares
+  const size_t res_total = std::min<size_t>(B * p->res_blocks_per_seq, p->mode == KVS_MODE_H2O ? NP : SIZE_MAX);
+  const size_t gen = B * Hq * (size_t)p->res_blocks_per_seq * kBlock;
+  const size_t tcs = (res_total + 2 * (size_t)kGridMax) * Hq * kBlock;
+  p->logit_elems = std::max(gen, tcs);
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
+  p->k_pages = take(L * NP * p->page_bytes);
+  p->v_pages = take(L * NP * p->page_bytes);
+  const bool fp8 = c->kv_dtype == KVS_E4M3;
+  p->k_scales = take(fp8 ? L * slots * 4 : 0);
+  p->v_scales = take(fp8 ? L * slots * 4 : 0);
+  p->pos = take(L * slots * 8);
+  p->tok_mass = take(L * slots * 4);
+  p->blk_mass = take(L * B * MB * 4);
+  p->next_pos = take(L * B * 8);
+  p->app_tickets = take(L * B * 4);
+  p->block_table = take(B * MB * 4);
+  p->res_blocks = take(B * MB * 4);
+  p->res_pages = take(B * MB * 4);
+  p->res_count = take(B * 4);
+  p->free_pages = take(NP * 4);
+  p->free_top = take(4);
+  p->c_tok = take(B * P * 8);
+  p->e_tok = take(B * P * 8);
+  p->last_tok = take(B * P * 4);
+  p->c_blk = take(B * MB * 8);
+  p->e_blk = take(B * MB * 8);
+  p->last_blk = take(B * MB * 4);
+  p->steps = take(B * 4);
+  p->acc_tickets = take(B * 4);
+  p->partials = take(((size_t)kGridMax + B) * Hq * (D + 2) * 4);
+  p->counters = take(2 * B * 4);
+  p->logits = take(p->logit_elems * 4);
+  p->err = take(4);
+  p->total = o;
+}
+
+}  // namespace
+
+struct kvs_ctx {
+  kvs_config cfg;
+  Plan plan;
+  Dev dev;
+  int device = 0, sm_count = 0, kernel = KVS_KERNEL_GENERAL, grid = 0;
+  std::vector<int64_t> next;        // [L][max_seqs]
+  std::vector<int64_t> frontier;    // [max_seqs] max over layers of next (pages allocated below it)
+  std::vector<int64_t> h2o_bound;   // [max_seqs] bound on resident blocks (H2O)
+  std::vector<CUtensorMap> maps;    // [L][2]
+  std::string err;
+};
+
+namespace {
+
+kvs_status fail(kvs_ctx* ctx, kvs_status s, const char* fmt, ...) {
+  if (ctx) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    ctx->err = buf;
+  }
+  return s;
+}
+
+kvs_status cuda_ok(kvs_ctx* ctx, cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return KVS_OK;
+  return fail(ctx, KVS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+kvs_status check_range(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs) {
+  if (n_seqs < 1 || seq_begin < 0 || (int64_t)seq_begin + n_seqs > ctx->cfg.max_seqs)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence range [%d, %d) outside [0, %d)", seq_begin,
+                seq_begin + n_seqs, ctx->cfg.max_seqs);
+  return KVS_OK;
+}
+
+int64_t seq_block_bound(const kvs_ctx* ctx, int s) {
+  if (ctx->plan.mode == KVS_MODE_H2O)
+    return std::min<int64_t>(ctx->plan.max_blocks, ctx->h2o_bound[s] + 2);
+  return ctx->plan.res_blocks_per_seq;
+}
+
+}  // namespace
+
+extern "C" {
+
+void kvs_config_init(kvs_config* cfg) {
+  if (!cfg) return;
+  std::memset(cfg, 0, sizeof *cfg);
+  cfg->num_layers = 1;
+  cfg->num_q_heads = 8;
+  cfg->num_kv_heads = 1;
+  cfg->head_dim = 128;
+  cfg->max_seqs = 1;
+  cfg->max_positions = 4096;
+  cfg->block_tokens = kBlock;
+  cfg->h2o_sink_tokens = 4;
+  cfg->h2o_recent_frac = 0.25;
+  cfg->ema_decay = 0.9;
+  cfg->kv_dtype = KVS_BF16;
+  cfg->in_dtype = KVS_BF16;
+}
+
+kvs_status kvs_validate_config(const kvs_config* cfg, char* msg, size_t msg_len) {
+  return check_config(cfg, msg, msg_len);
+}
+
+size_t kvs_workspace_bytes(const kvs_config* cfg) {
+  if (check_config(cfg, nullptr, 0) != KVS_OK) return 0;
+  Plan p;
+  make_plan(cfg, &p);
+  return p.total;
+}
+
+kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace_bytes, kvs_stream_t stream,
+                      kvs_ctx** out) {
+  if (!out) return KVS_ERR_INVALID_ARGUMENT;
+  *out = nullptr;
+  char msg[256];
+  kvs_status st = check_config(cfg, msg, sizeof msg);
+  if (st != KVS_OK) return st;
+  Plan p;
+  make_plan(cfg, &p);
+  if (!d_workspace || (reinterpret_cast<uintptr_t>(d_workspace) & 255)) return KVS_ERR_INVALID_ARGUMENT;
+  if (workspace_bytes < p.total) return KVS_ERR_CAPACITY;
+  kvs_ctx* ctx = new (std::nothrow) kvs_ctx();
+  if (!ctx) return KVS_ERR_CAPACITY;
+  ctx->cfg = *cfg;
+  ctx->plan = p;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaGetDevice(&ctx->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ctx->sm_count, cudaDevAttrMultiProcessorCount, ctx->device) != cudaSuccess) {
+    delete ctx;
+    return KVS_ERR_CUDA;
+  }
+  uint8_t* w = static_cast<uint8_t*>(d_workspace);
+  Dev& d = ctx->dev;
+  std::memset(&d, 0, sizeof d);
+  d.L = cfg->num_layers; d.Hq = cfg->num_q_heads; d.Hkv = cfg->num_kv_heads; d.D = cfg->head_dim;
+  d.G = cfg->num_q_heads / cfg->num_kv_heads;
+  d.max_seqs = cfg->max_seqs; d.max_positions = cfg->max_positions; d.max_blocks = p.max_blocks;
+  d.window = cfg->window; d.mode = p.mode; d.num_pages = p.num_pages; d.pages_per_seq = p.pages_per_seq;
+  d.kv_dtype = cfg->kv_dtype; d.in_dtype = cfg->in_dtype;
+  d.spin_limit = cfg->spin_limit == 0 ? kDefaultSpin : (cfg->spin_limit < 0 ? 0 : cfg->spin_limit);
+  d.h2o_sink_tokens = cfg->h2o_sink_tokens; d.h2o_recent_tokens = p.recent_tokens;
+  d.ema_decay = cfg->ema_decay;
+  const size_t slots = (size_t)p.num_pages * kBlock;
+  d.k_pages = w + p.k_pages; d.v_pages = w + p.v_pages;
+  d.page_layer_bytes = (size_t)p.num_pages * p.page_bytes; d.page_bytes = p.page_bytes;
+  d.k_scales = cfg->kv_dtype == KVS_E4M3 ? reinterpret_cast<float*>(w + p.k_scales) : nullptr;
+  d.v_scales = cfg->kv_dtype == KVS_E4M3 ? reinterpret_cast<float*>(w + p.v_scales) : nullptr;
+  d.slot_layer_elems = slots;
+  d.pos = reinterpret_cast<int64_t*>(w + p.pos);
+  d.tok_mass = reinterpret_cast<float*>(w + p.tok_mass);
+  d.blk_mass = reinterpret_cast<float*>(w + p.blk_mass);
+  d.blk_layer_elems = (size_t)cfg->max_seqs * p.max_blocks;
+  d.next_pos = reinterpret_cast<int64_t*>(w + p.next_pos);
+  d.append_tickets = reinterpret_cast<int32_t*>(w + p.app_tickets);
+  d.block_table = reinterpret_cast<int32_t*>(w + p.block_table);
+  d.res_blocks = reinterpret_cast<int32_t*>(w + p.res_blocks);
+  d.res_pages = reinterpret_cast<int32_t*>(w + p.res_pages);
+  d.res_count = reinterpret_cast<int32_t*>(w + p.res_count);
+  d.free_pages = reinterpret_cast<int32_t*>(w + p.free_pages);
+  d.free_top = reinterpret_cast<int32_t*>(w + p.free_top);
+  d.c_tok = reinterpret_cast<double*>(w + p.c_tok);
+  d.e_tok = reinterpret_cast<double*>(w + p.e_tok);
+  d.last_tok = reinterpret_cast<int32_t*>(w + p.last_tok);
+  d.c_blk = reinterpret_cast<double*>(w + p.c_blk);
+  d.e_blk = reinterpret_cast<double*>(w + p.e_blk);
+  d.last_blk = reinterpret_cast<int32_t*>(w + p.last_blk);
+  d.steps = reinterpret_cast<int32_t*>(w + p.steps);
+  d.acc_tickets = reinterpret_cast<int32_t*>(w + p.acc_tickets);
+  d.partials = reinterpret_cast<float*>(w + p.partials);
+  d.counters = reinterpret_cast<int32_t*>(w + p.counters);
+  d.logit_scratch = reinterpret_cast<float*>(w + p.logits);
+  d.logit_scratch_elems = p.logit_elems;
+  d.err = reinterpret_cast<int32_t*>(w + p.err);
+
+  const bool tc = tc_supported(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim, cfg->kv_dtype, cfg->in_dtype,
+                               cfg->window, p.mode);
+  ctx->kernel = (cfg->kernel == KVS_KERNEL_GENERAL || !tc) ? KVS_KERNEL_GENERAL : KVS_KERNEL_TENSOR;
+  if (ctx->kernel == KVS_KERNEL_TENSOR) {
+    ctx->grid = tc_grid(cfg->kv_dtype, cfg->num_kv_heads, ctx->sm_count);
+    if (ctx->grid < 1) {
+      delete ctx;
+      return KVS_ERR_CUDA;
+    }
+    ctx->maps.resize((size_t)cfg->num_layers * 2);
+    for (int l = 0; l < cfg->num_layers; ++l) {
+      if (make_page_map(&ctx->maps[2 * l], d.k_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype) != cudaSuccess ||
+          make_page_map(&ctx->maps[2 * l + 1], d.v_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype) != cudaSuccess) {
+        delete ctx;
+        return KVS_ERR_CUDA;
+      }
+    }
+  }
+  ctx->next.assign((size_t)cfg->num_layers * cfg->max_seqs, 0);
+  ctx->frontier.assign(cfg->max_seqs, 0);
+  ctx->h2o_bound.assign(cfg->max_seqs, 0);
+  if (cudaMemsetAsync(d_workspace, 0, p.total, s) != cudaSuccess || launch_init(d, s) != cudaSuccess) {
+    delete ctx;
+    return KVS_ERR_CUDA;
+  }
+  *out = ctx;
+  return KVS_OK;
+}
+
+kvs_status kvs_destroy(kvs_ctx* ctx) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  delete ctx;
+  return KVS_OK;
+}
+
+kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  st = cuda_ok(ctx, launch_reset(ctx->dev, seq_begin, n_seqs, reinterpret_cast<cudaStream_t>(stream)), "reset");
+  if (st != KVS_OK) return st;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    for (int l = 0; l < ctx->cfg.num_layers; ++l) ctx->next[(size_t)l * ctx->cfg.max_seqs + s] = 0;
+    ctx->frontier[s] = 0;
+    ctx->h2o_bound[s] = 0;
+  }
+  return KVS_OK;
+}
+
+kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, int32_t n_new,
+                         const void* d_k, const void* d_v, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (n_new < 1) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "n_new must be >= 1");
+  if (!d_k || !d_v) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL K or V");
+  const int B = ctx->cfg.max_seqs;
+  bool lead = false;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    const int64_t nx = ctx->next[(size_t)layer * B + s];
+    if (nx + n_new > ctx->cfg.max_positions)
+      return fail(ctx, KVS_ERR_CAPACITY, "sequence %d: position %lld + %d exceeds max_positions %d", s,
+                  (long long)nx, n_new, ctx->cfg.max_positions);
+    if (nx + n_new > ctx->frontier[s]) lead = true;
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (ctx->plan.mode == KVS_MODE_H2O && lead) {
+    st = cuda_ok(ctx, launch_alloc_pages(ctx->dev, layer, seq_begin, n_seqs, n_new, cs), "page allocation");
+    if (st != KVS_OK) return st;
+  }
+  st = cuda_ok(ctx, launch_append(ctx->dev, layer, seq_begin, n_seqs, n_new, d_k, d_v, cs), "append");
+  if (st != KVS_OK) return st;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    int64_t& nx = ctx->next[(size_t)layer * B + s];
+    nx += n_new;
+    if (nx > ctx->frontier[s]) {
+      const int64_t new_blocks = cdiv64(nx, kBlock) - cdiv64(ctx->frontier[s], kBlock);
+      ctx->h2o_bound[s] += new_blocks;
+      ctx->frontier[s] = nx;
+    }
+  }
+  return KVS_OK;
+}
+
+kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_q,
+                             float* d_out, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  const int B = ctx->cfg.max_seqs;
+  int64_t T_bound = 0;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    if (ctx->next[(size_t)layer * B + s] == 0)
+      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
+    T_bound += seq_block_bound(ctx, s);
+  }
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (ctx->kernel == KVS_KERNEL_TENSOR) {
+    return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
+                                         n_seqs, d_q, d_out, T_bound, ctx->grid, cs),
+                   "tensor-core attend");
+  }
+  return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
+}
+
+kvs_status kvs_accumulate_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  const int B = ctx->cfg.max_seqs;
+  int64_t maxb = 1;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    const int64_t n0 = ctx->next[s];
+    for (int l = 1; l < ctx->cfg.num_layers; ++l)
+      if (ctx->next[(size_t)l * B + s] != n0)
+        return fail(ctx, KVS_ERR_STATE, "sequence %d: layers disagree on next_position", s);
+    maxb = std::max(maxb, seq_block_bound(ctx, s));
+  }
+  return cuda_ok(ctx, launch_accumulate(ctx->dev, seq_begin, n_seqs, (int)maxb, reinterpret_cast<cudaStream_t>(stream)),
+                 "accumulate");
+}
+
+kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const int32_t* d_k_per_seq,
+                             int32_t k_uniform, int32_t score_kind, uint32_t flags, int32_t* d_keep_ids,
+                             int32_t keep_capacity, int32_t* d_keep_count, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (score_kind != KVS_SCORE_CUMULATIVE && score_kind != KVS_SCORE_EMA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE or EMA");
+  if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
+  if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
+  if (!d_k_per_seq && k_uniform < 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "k must be >= 0");
+  if (!d_keep_ids || !d_keep_count || keep_capacity < 1)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "keep buffers missing or keep_capacity < 1");
+  st = cuda_ok(ctx, launch_select(ctx->dev, seq_begin, n_seqs, d_k_per_seq, k_uniform, score_kind, flags, d_keep_ids,
+                                  keep_capacity, d_keep_count, reinterpret_cast<cudaStream_t>(stream)),
+               "select");
+  if (st != KVS_OK) return st;
+  if ((flags & KVS_SELECT_APPLY) && !d_k_per_seq) {
+    // kept <= max(k, protected blocks); protected <= sink blocks + recent blocks + 1
+    const int64_t prot = cdiv64(ctx->cfg.h2o_sink_tokens, kBlock) + cdiv64(ctx->plan.recent_tokens, kBlock) + 1;
+    const int64_t kept = std::max<int64_t>(k_uniform, (flags & KVS_SELECT_PROTECT) ? prot : 0);
+    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) ctx->h2o_bound[s] = std::min(ctx->h2o_bound[s], kept);
+  }
+  return KVS_OK;
+}
+
+size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
+  if (!ctx) return 0;
+  const size_t slots = (size_t)ctx->plan.num_pages * kBlock, B = ctx->cfg.max_seqs, MB = ctx->plan.max_blocks;
+  switch (what) {
+    case KVS_STATE_K_PAGES: case KVS_STATE_V_PAGES: return (size_t)ctx->plan.num_pages * ctx->plan.page_bytes;
+    case KVS_STATE_K_SCALES: case KVS_STATE_V_SCALES: return ctx->cfg.kv_dtype == KVS_E4M3 ? slots * 4 : 0;
+    case KVS_STATE_POSITIONS: return slots * 8;
+    case KVS_STATE_NEXT_POSITION: return B * 8;
+    case KVS_STATE_TOKEN_MASS: return slots * 4;
+    case KVS_STATE_BLOCK_MASS: return B * MB * 4;
+    case KVS_STATE_C_TOKEN: case KVS_STATE_E_TOKEN: return B * ctx->cfg.max_positions * 8;
+    case KVS_STATE_C_BLOCK: case KVS_STATE_E_BLOCK: return B * MB * 8;
+    case KVS_STATE_STEPS: return B * 4;
+    case KVS_STATE_BLOCK_TABLE: return B * MB * 4;
+    default: return 0;
+  }
+}
+
+kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst, size_t dst_bytes,
+                          kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  const size_t n = kvs_state_bytes(ctx, what);
+  if (n == 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "state item %d not available", what);
+  if (!d_dst || dst_bytes < n) return fail(ctx, KVS_ERR_CAPACITY, "destination needs %zu bytes", n);
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  const Dev& d = ctx->dev;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const size_t slots = d.slot_layer_elems;
+  const void* src = nullptr;
+  switch (what) {
+    case KVS_STATE_K_PAGES: src = d.k_pages + layer * d.page_layer_bytes; break;
+    case KVS_STATE_V_PAGES: src = d.v_pages + layer * d.page_layer_bytes; break;
+    case KVS_STATE_K_SCALES: src = d.k_scales + layer * slots; break;
+    case KVS_STATE_V_SCALES: src = d.v_scales + layer * slots; break;
+    case KVS_STATE_POSITIONS: src = d.pos + layer * slots; break;
+    case KVS_STATE_NEXT_POSITION: src = d.next_pos + (size_t)layer * d.max_seqs; break;
+    case KVS_STATE_TOKEN_MASS: src = d.tok_mass + layer * slots; break;
+    case KVS_STATE_BLOCK_MASS: src = d.blk_mass + layer * d.blk_layer_elems; break;
+    case KVS_STATE_C_TOKEN: src = d.c_tok; break;
+    case KVS_STATE_C_BLOCK: src = d.c_blk; break;
+    case KVS_STATE_STEPS: src = d.steps; break;
+    case KVS_STATE_BLOCK_TABLE: src = d.block_table; break;
+    case KVS_STATE_E_TOKEN: case KVS_STATE_E_BLOCK:
+      return cuda_ok(ctx, launch_read_ema(d, what, static_cast<double*>(d_dst), cs), "read EMA");
+    default: return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "state item %d", what);
+  }
+  return cuda_ok(ctx, cudaMemcpyAsync(d_dst, src, n, cudaMemcpyDeviceToDevice, cs), "read state");
+}
+
+kvs_status kvs_get_layout(const kvs_ctx* ctx, kvs_layout* out) {
+  if (!ctx || !out) return KVS_ERR_INVALID_ARGUMENT;
+  std::memset(out, 0, sizeof *out);
+  out->mode = ctx->plan.mode;
+  out->num_pages = ctx->plan.num_pages;
+  out->pages_per_seq = ctx->plan.pages_per_seq;
+  out->max_blocks = ctx->plan.max_blocks;
+  out->attend_kernel = ctx->kernel;
+  out->attend_grid = ctx->grid;
+  return KVS_OK;
+}
+
+kvs_status kvs_get_status(kvs_ctx* ctx, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  kvs_status st = cuda_ok(ctx, cudaStreamSynchronize(cs), "synchronise");
+  if (st != KVS_OK) return st;
+  int32_t e = 0;
+  st = cuda_ok(ctx, cudaMemcpy(&e, ctx->dev.err, 4, cudaMemcpyDeviceToHost), "read error word");
+  if (st != KVS_OK) return st;
+  if (e & kErrTimeout) return fail(ctx, KVS_ERR_TIMEOUT, "a device-side wait ran out (error word 0x%x)", e);
+  if (e & kErrCapacity) return fail(ctx, KVS_ERR_CAPACITY, "device capacity exhausted (error word 0x%x)", e);
+  if (e & kErrState) return fail(ctx, KVS_ERR_STATE, "inconsistent device state (error word 0x%x)", e);
+  return KVS_OK;
+}
+
+kvs_status kvs_clear_error(kvs_ctx* ctx, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  return cuda_ok(ctx, launch_clear(ctx->dev, reinterpret_cast<cudaStream_t>(stream)), "clear error");
+}
+
+const char* kvs_last_error(const kvs_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
+
+const char* kvs_status_string(kvs_status s) {
+  switch (s) {
+    case KVS_OK: return "ok";
+    case KVS_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KVS_ERR_CAPACITY: return "capacity exceeded";
+    case KVS_ERR_EMPTY_CACHE: return "empty cache (all-masked row)";
+    case KVS_ERR_CUDA: return "CUDA error";
+    case KVS_ERR_TIMEOUT: return "device wait timed out";
+    case KVS_ERR_UNSUPPORTED: return "unsupported";
+    case KVS_ERR_STATE: return "call order violated";
+    default: return "unknown status";
+  }
+}
+
+int32_t kvs_abi_version(void) { return KVS_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,164 @@
+// Internal declarations shared by the CUDA translation units of libkvs.
+//
+// Workspace layout (all regions 256-byte aligned, owned by the caller):
+//   per layer l (stride = layer_bytes of each array):
+//     K pages, V pages   [num_pages][Hkv][16][D] storage elements
+//     K, V scales        [num_pages][16] float        (E4M3 only)
+//     positions          [num_pages][16] int64         (-1 = empty slot)
+//     token masses       [num_pages][16] float         (entry masses of the last attend)
+//     block masses       [max_seqs][max_blocks] float  (block masses of the last attend)
+//     next_position      [max_seqs] int64
+//     append tickets     [max_seqs] int32
+//   shared by all layers:
+//     block table, resident block list, resident page list [max_seqs][max_blocks] int32
+//     resident count [max_seqs]; free page stack [num_pages] + top
+//     score tables C/E per token [max_seqs][max_positions] double, stamp int32;
+//     C/E per block [max_seqs][max_blocks] double, stamp int32; steps [max_seqs] int32
+//     attend partials [(grid_max + max_seqs)][Hq][D + 2] float; arrival counters
+//     logit scratch (the general kernel, and the tensor kernel when logits do not fit
+//     in shared memory); accumulate tickets; the error word.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/kvs.h"
+
+namespace kvs {
+
+constexpr int kBlock = 16;          // tokens per block (placement unit)
+constexpr int kGridMax = 256;       // upper bound of persistent attend CTAs (sizing)
+
+// Device error word bits.
+enum : int32_t {
+  kErrCapacity = 1,      // H2O page pool empty / position overflow seen on device
+  kErrTimeout = 2,       // a bounded wait ran out
+  kErrState = 4,         // missing page / inconsistent state seen on device
+};
+
+struct Dev {
+  // shape
+  int32_t L, Hq, Hkv, D, G;
+  int32_t max_seqs, max_positions, max_blocks;
+  int32_t window, mode, num_pages, pages_per_seq;
+  int32_t kv_dtype, in_dtype;
+  int32_t spin_limit;
+  int32_t h2o_sink_tokens, h2o_recent_tokens;
+  double ema_decay;
+  // per-layer arrays: base pointer + per-layer stride in elements
+  uint8_t* k_pages;  uint8_t* v_pages;  size_t page_layer_bytes;  size_t page_bytes;
+  float* k_scales;   float* v_scales;   size_t slot_layer_elems;   // num_pages*16
+  int64_t* pos;
+  float* tok_mass;
+  float* blk_mass;   size_t blk_layer_elems;                       // max_seqs*max_blocks
+  int64_t* next_pos;                                               // [L][max_seqs]
+  int32_t* append_tickets;                                         // [L][max_seqs]
+  // shared
+  int32_t* block_table;   // [max_seqs][max_blocks]
+  int32_t* res_blocks;    // [max_seqs][max_blocks]
+  int32_t* res_pages;     // [max_seqs][max_blocks]
+  int32_t* res_count;     // [max_seqs]
+  int32_t* free_pages;    // [num_pages]
+  int32_t* free_top;      // [1]
+  double* c_tok; double* e_tok; int32_t* last_tok;   // [max_seqs][max_positions]
+  double* c_blk; double* e_blk; int32_t* last_blk;   // [max_seqs][max_blocks]
+  int32_t* steps;                                    // [max_seqs]
+  int32_t* acc_tickets;                              // [max_seqs]
+  float* partials;        // [(kGridMax + max_seqs)][Hq][D + 2]
+  int32_t* counters;      // [2][max_seqs] arrivals, departures
+  float* logit_scratch;   size_t logit_scratch_elems;
+  int32_t* err;           // [1]
+};
+
+__host__ __device__ inline int64_t cdiv64(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Storage location of absolute position p of sequence s: page and slot in page.
+__device__ __forceinline__ int32_t page_of(const Dev& d, int s, int64_t p, int32_t* slot) {
+  if (d.mode == KVS_MODE_WINDOW) {
+    int64_t w = p % d.window;
+    *slot = (int32_t)(w % kBlock);
+    return s * d.pages_per_seq + (int32_t)(w / kBlock);
+  }
+  *slot = (int32_t)(p % kBlock);
+  if (d.mode == KVS_MODE_H2O) return d.block_table[(size_t)s * d.max_blocks + p / kBlock];
+  return s * d.pages_per_seq + (int32_t)(p / kBlock);
+}
+
+// Resident block range of sequence s given next position nxt.
+//   NONE / WINDOW: blocks [k0, k0 + n) contiguous in block id; H2O: the resident list.
+struct SeqBlocks {
+  int64_t next, lo;   // resident positions are lo <= p < next (H2O: within listed blocks)
+  int32_t k0, n;      // first block id and block count (H2O: k0 unused)
+};
+
+__device__ __forceinline__ SeqBlocks seq_blocks(const Dev& d, int layer, int s) {
+  SeqBlocks r;
+  r.next = d.next_pos[(size_t)layer * d.max_seqs + s];
+  r.lo = 0;
+  if (d.mode == KVS_MODE_WINDOW && r.next > d.window) r.lo = r.next - d.window;
+  if (r.next <= 0) { r.k0 = 0; r.n = 0; return r; }
+  if (d.mode == KVS_MODE_H2O) { r.k0 = 0; r.n = d.res_count[s]; return r; }
+  r.k0 = (int32_t)(r.lo / kBlock);
+  r.n = (int32_t)((r.next - 1) / kBlock) - r.k0 + 1;
+  return r;
+}
+
+// Block id and page of the i-th resident block of sequence s.
+__device__ __forceinline__ int32_t block_at(const Dev& d, int s, const SeqBlocks& sb, int i,
+                                            int32_t* page) {
+  if (d.mode == KVS_MODE_H2O) {
+    *page = d.res_pages[(size_t)s * d.max_blocks + i];
+    return d.res_blocks[(size_t)s * d.max_blocks + i];
+  }
+  int32_t k = sb.k0 + i;
+  int32_t idx = (d.mode == KVS_MODE_WINDOW) ? (k % d.pages_per_seq) : k;
+  *page = s * d.pages_per_seq + idx;
+  return k;
+}
+
+__device__ __forceinline__ void set_error(const Dev& d, int32_t bits) { atomicOr(d.err, bits); }
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
+  int32_t v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Poll *p until it reaches target, at most `limit` sleeps (limit 0: one look only).
+// Returns false when the limit ran out (the caller records kErrTimeout).
+__device__ __forceinline__ bool wait_at_least(const int32_t* p, int32_t target, int32_t limit) {
+  for (int32_t it = 0;; ++it) {
+    if (ld_acquire(p) >= target) return true;
+    if (it >= limit) return false;
+    __nanosleep(100);
+  }
+}
+
+}  // namespace kvs
+
+// Host-side entry points of each translation unit (launchers).
+namespace kvs {
+struct Ctx;
+cudaError_t launch_init(const Dev& d, cudaStream_t st);
+cudaError_t launch_reset(const Dev& d, int seq_begin, int n_seqs, cudaStream_t st);
+cudaError_t launch_alloc_pages(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+                               cudaStream_t st);
+cudaError_t launch_append(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+                          const void* k, const void* v, cudaStream_t st);
+cudaError_t launch_attend_general(const Dev& d, int layer, int seq_begin, int n_seqs,
+                                  const void* q, float* out, cudaStream_t st);
+cudaError_t launch_accumulate(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+                              cudaStream_t st);
+cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,
+                          int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
+                          int32_t* keep_count, cudaStream_t st);
+cudaError_t launch_read_ema(const Dev& d, int what, double* dst, cudaStream_t st);
+cudaError_t launch_clear(const Dev& d, cudaStream_t st);
+size_t general_smem_bytes(int Hq, int D);
+}  // namespace kvs

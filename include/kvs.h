@@ -1,0 +1,251 @@
+/*
+ * kvs.h - C ABI of the attention-scored KV cache decode path (GB300, sm_103a).
+ *
+ * One decode step over a KV cache that also scores what it attends:
+ *
+ *   for every layer l:  kvs_append_kv     store the new token's K and V
+ *                       kvs_decode_attend attend every query head over the resident
+ *                                         entries, write the output, and turn the
+ *                                         post-softmax weights into per-token and
+ *                                         per-16-token-block masses on chip
+ *   once per step:      kvs_accumulate_scores  cumulative + EMA score tables
+ *                       kvs_select_blocks      top-k blocks to keep resident
+ *
+ * Sources (page title, then section):
+ *   - Flash-MoE "Context Optimization": FP8 KV Cache > How It Works (E4M3 codes, one
+ *     scale = absmax/240 per position, decoded inline during attention); Flag
+ *     Ordering (the storage format is fixed before set-up); Sliding Window Attention >
+ *     Design (circular slot = position % window); H2O KV Cache Eviction (sink, recent
+ *     and heavy-hitter regions; score = post-softmax weights summed over all query
+ *     heads and steps); H2O vs Sliding Window (H2O takes priority).
+ *   - "Context views at marginal cost": Tier 1 (keep a running reduction - EMA and
+ *     cumulative - never the attention matrix); Fact 3 (the QK^T, softmax, V read is
+ *     the floor of the method).
+ *   - "Per-Head Attention as a Scoring Signal": Fix: score per head, place per block
+ *     (a block of 16 tokens stays if any head weights it).
+ *   - "LLM mechanics III": sections 1, 3 and 5 (the window includes the current
+ *     token; slots, absolute positions and the processed count are kept apart;
+ *     invalid windows and all-masked rows are rejected).
+ *
+ * Conventions
+ *   - Every call returns a kvs_status; nothing is thrown across the ABI.  Arguments
+ *     are checked on the host before any launch; a call that fails a check launches
+ *     nothing and leaves the state unchanged.  kvs_last_error() describes the last
+ *     failure of a context.
+ *   - Device memory is owned by the caller: kvs_create() takes a workspace of
+ *     kvs_workspace_bytes() bytes and keeps non-owning pointers into it until
+ *     kvs_destroy().  The library itself never allocates device memory.
+ *   - Pointers named d_* are device pointers; h_* are host pointers.  Every launch
+ *     goes on the stream given to the call (a cudaStream_t; 0 is the legacy default
+ *     stream).  No call synchronises except kvs_get_status().
+ *   - Device-side failures (capacity exhausted, a bounded wait that ran out) set an
+ *     error word that kvs_get_status() reports and kvs_clear_error() resets.
+ *   - Sequences are addressed as a contiguous range [seq_begin, seq_begin + n_seqs)
+ *     of the max_seqs sequences the cache holds; per-sequence inputs and outputs are
+ *     packed in that order.
+ *   - Call order per step: kvs_append_kv(l) before kvs_decode_attend(l) for every
+ *     layer, kvs_accumulate_scores() after the last layer, then kvs_select_blocks().
+ */
+#ifndef KVS_H
+#define KVS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVS_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define KVS_API __attribute__((visibility("default")))
+#else
+#define KVS_API
+#endif
+
+typedef struct kvs_ctx kvs_ctx;
+typedef struct CUstream_st* kvs_stream_t;   /* a cudaStream_t */
+
+typedef enum {
+  KVS_OK = 0,
+  KVS_ERR_INVALID_ARGUMENT = 1, /* a bad pointer, size, id, window or config field */
+  KVS_ERR_CAPACITY = 2,         /* positions, pages or an output buffer would overflow */
+  KVS_ERR_EMPTY_CACHE = 3,      /* attend with no resident entry: an all-masked row */
+  KVS_ERR_CUDA = 4,             /* a CUDA runtime call failed */
+  KVS_ERR_TIMEOUT = 5,          /* a device-side bounded wait ran out */
+  KVS_ERR_UNSUPPORTED = 6,      /* shape or format not covered by any kernel */
+  KVS_ERR_STATE = 7             /* call order violated (e.g. layers disagree) */
+} kvs_status;
+
+typedef enum { KVS_F32 = 0, KVS_BF16 = 1, KVS_E4M3 = 2 } kvs_dtype;
+
+typedef enum { KVS_SCORE_CUMULATIVE = 0, KVS_SCORE_EMA = 1 } kvs_score_kind;
+
+/* Attend kernel choice: AUTO takes the tensor-core kernel when the shape allows it
+ * (head_dim 128, 8 query heads per KV head, bf16 inputs, bf16 or E4M3 storage, and
+ * a window that is 0 or a multiple of 16), else the general CUDA-core kernel. */
+typedef enum { KVS_KERNEL_AUTO = 0, KVS_KERNEL_GENERAL = 1, KVS_KERNEL_TENSOR = 2 } kvs_kernel;
+
+/* Residency mode, derived from the config: H2O when h2o_budget_tokens > 0 (it takes
+ * priority over a window), else WINDOW when window > 0, else NONE. */
+typedef enum { KVS_MODE_NONE = 0, KVS_MODE_WINDOW = 1, KVS_MODE_H2O = 2 } kvs_mode;
+
+typedef struct {
+  int32_t num_layers;        /* >= 1 */
+  int32_t num_q_heads;       /* Hq, a multiple of num_kv_heads */
+  int32_t num_kv_heads;      /* Hkv; query head h reads KV head h / (Hq / Hkv) */
+  int32_t head_dim;          /* D in {16, 32, 64, 128} */
+  int32_t max_seqs;          /* sequences held */
+  int32_t max_positions;     /* absolute-position capacity of each sequence */
+  int32_t window;            /* 0 = none; else >= 1 positions, the current one included */
+  int32_t block_tokens;      /* 16 (the only value supported) */
+  int32_t h2o_budget_tokens; /* 0 = off; else the resident budget (a multiple of 16) */
+  int32_t h2o_sink_tokens;   /* H2O: always keep the blocks of the first N tokens (4) */
+  int32_t num_pages;         /* H2O page pool (0 = max_seqs * ceil(max_positions/16)) */
+  int32_t kernel;            /* a kvs_kernel */
+  int32_t spin_limit;        /* device wait polls: 0 = default (~0.5 s), > 0 = that many, -1 = no poll
+                                (a CTA that is not the last to arrive reports KVS_ERR_TIMEOUT) */
+  int32_t kv_dtype;          /* storage: KVS_F32, KVS_BF16 or KVS_E4M3 */
+  int32_t in_dtype;          /* dtype of Q, K, V inputs: KVS_F32 or KVS_BF16 */
+  int32_t reserved_i[5];     /* must be 0 */
+  double  h2o_recent_frac;   /* H2O: always keep the last frac * budget tokens (0.25) */
+  double  ema_decay;         /* d in E <- d*E + (1-d)*x, in [0, 1) (0.9) */
+  double  reserved_d[2];     /* must be 0 */
+} kvs_config;
+
+/* Fill *cfg with defaults (block 16, sinks 4, recent 0.25, decay 0.9, bf16). */
+KVS_API void kvs_config_init(kvs_config* cfg);
+
+/* Check a config without touching the GPU.  On failure writes a message into msg
+ * (if msg_len > 0) and returns KVS_ERR_INVALID_ARGUMENT or KVS_ERR_UNSUPPORTED. */
+KVS_API kvs_status kvs_validate_config(const kvs_config* cfg, char* msg, size_t msg_len);
+
+/* Workspace bytes a config needs (0 if the config is invalid).  Host-only. */
+KVS_API size_t kvs_workspace_bytes(const kvs_config* cfg);
+
+/* Bind a context to a caller-owned device workspace of at least
+ * kvs_workspace_bytes(cfg) bytes (256-byte aligned) on the current device and
+ * initialise it (on `stream`).  The config is copied and fixed for the context's
+ * life: the storage format decides the workspace layout.  *out receives the
+ * context (a host object; free it with kvs_destroy). */
+KVS_API kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace_bytes,
+                      kvs_stream_t stream, kvs_ctx** out);
+
+/* Free the host object.  The workspace stays the caller's. */
+KVS_API kvs_status kvs_destroy(kvs_ctx* ctx);
+
+/* Empty sequences [seq_begin, seq_begin + n_seqs): next_position = 0 in every
+ * layer, score tables zeroed, H2O pages returned to the pool. */
+KVS_API kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream);
+
+/* Append n_new tokens to every sequence of the range in layer `layer`.
+ * d_k, d_v: [n_seqs][n_new][num_kv_heads][head_dim] in in_dtype, device memory.
+ * Token i of sequence s goes to absolute position next_position[layer][s] + i.
+ * E4M3 storage quantises each position (all KV heads of one of K or V) with
+ * scale = fl32(absmax / 240) and round-to-nearest-even saturating E4M3 codes of
+ * fl32(x / scale); absmax 0 gives scale 0 and zero codes.
+ * Window mode writes position p to slot p % window; H2O mode writes it to the page
+ * of block p / 16.  Errors: KVS_ERR_CAPACITY if a sequence would pass
+ * max_positions (or, on the device, if the H2O page pool is empty). */
+KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                         int32_t n_new, const void* d_k, const void* d_v, kvs_stream_t stream);
+
+/* Decode attention of one query per head over the resident entries of layer `layer`.
+ * d_q: [n_seqs][num_q_heads][head_dim] in in_dtype; d_out: [n_seqs][num_q_heads]
+ * [head_dim] float32, both device memory.  Logits are q.k/sqrt(D) (k, v decoded
+ * inline from E4M3 as code * scale), softmax per head over the resident entries.
+ * In the same launch, without writing the weights anywhere off chip, the kernel
+ * stores the step masses of this layer: per resident entry the sum over query heads
+ * of its weight, and per resident 16-token block the maximum over query heads of
+ * the head's summed weight in the block (both readable with kvs_read_state).
+ * Errors: KVS_ERR_EMPTY_CACHE if a sequence of the range has no resident entry. */
+KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                             const void* d_q, float* d_out, kvs_stream_t stream);
+
+/* Fold this step's masses of every layer into the score tables of the range:
+ * token score x_p = sum over layers of the entry masses, block score y_k = max over
+ * layers of the block masses; for every tracked entry (every position below
+ * next_position and every block holding one) C += x and E <- d*E + (1-d)*x, x = 0
+ * where nothing was attended this step.  Errors: KVS_ERR_STATE if the layers of a
+ * sequence disagree on next_position. */
+KVS_API kvs_status kvs_accumulate_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
+                                 kvs_stream_t stream);
+
+#define KVS_SELECT_PROTECT 1u  /* H2O: keep the sink and recent blocks first */
+#define KVS_SELECT_APPLY   2u  /* H2O: evict the unkept blocks (pages back to the pool) */
+
+/* Per sequence of the range, keep the k resident blocks with the highest score
+ * (C or E, a kvs_score_kind), ties to the lower block id; all are kept when k >= the
+ * resident count.  With KVS_SELECT_PROTECT the blocks holding a sink token (position
+ * < h2o_sink_tokens) or a recent token (position >= next_position - ceil(recent_frac
+ * * budget)) are kept whatever their score and the rest of k is filled by score; if
+ * they alone exceed k, all of them are kept.  k comes from d_k_per_seq ([n_seqs]
+ * int32, device) or, when d_k_per_seq is NULL, from k_uniform for every sequence.
+ * d_keep_ids: [n_seqs][keep_capacity] int32 (device), ascending block ids;
+ * d_keep_count: [n_seqs] int32 (device), the number kept (ids beyond keep_capacity
+ * are dropped and flag KVS_ERR_CAPACITY on the device).
+ * Errors: KVS_ERR_INVALID_ARGUMENT for APPLY outside H2O mode or a negative k. */
+KVS_API kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
+                             const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
+                             uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
+                             int32_t* d_keep_count, kvs_stream_t stream);
+
+/* State read-back (tests, inspection).  Copies one array of `layer` (ignored for
+ * per-sequence items) into d_dst (device), which must hold kvs_state_bytes(). */
+typedef enum {
+  KVS_STATE_K_PAGES = 0,     /* [num_pages][Hkv][16][D] storage elements of K */
+  KVS_STATE_V_PAGES = 1,     /* same for V */
+  KVS_STATE_K_SCALES = 2,    /* [num_pages][16] float32 (E4M3 only) */
+  KVS_STATE_V_SCALES = 3,
+  KVS_STATE_POSITIONS = 4,   /* [num_pages][16] int64 absolute position per slot, -1 empty */
+  KVS_STATE_NEXT_POSITION = 5, /* [max_seqs] int64 */
+  KVS_STATE_TOKEN_MASS = 6,  /* [num_pages][16] float32 entry masses of the last attend */
+  KVS_STATE_BLOCK_MASS = 7,  /* [max_seqs][max_blocks] float32 block masses of the last attend */
+  KVS_STATE_C_TOKEN = 8,     /* [max_seqs][max_positions] float64 cumulative */
+  KVS_STATE_E_TOKEN = 9,     /* [max_seqs][max_positions] float64 EMA, as of the last step */
+  KVS_STATE_C_BLOCK = 10,    /* [max_seqs][max_blocks] float64 */
+  KVS_STATE_E_BLOCK = 11,
+  KVS_STATE_STEPS = 12,      /* [max_seqs] int32 accumulate steps done */
+  KVS_STATE_BLOCK_TABLE = 13,/* [max_seqs][max_blocks] int32 page of each block, -1 = none */
+  KVS_STATE_COUNT = 14
+} kvs_state_item;
+
+KVS_API size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what);
+KVS_API kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst, size_t dst_bytes,
+                          kvs_stream_t stream);
+
+/* Layout facts: the page of (sequence s, position p) is
+ *   NONE:   s * pages_per_seq + p / 16                slot p % 16
+ *   WINDOW: s * pages_per_seq + (p % window) / 16     slot (p % window) % 16
+ *   H2O:    block_table[s][p / 16]                    slot p % 16          */
+typedef struct {
+  int32_t mode;              /* a kvs_mode */
+  int32_t num_pages;
+  int32_t pages_per_seq;     /* NONE and WINDOW modes */
+  int32_t max_blocks;        /* ceil(max_positions / 16) */
+  int32_t attend_kernel;     /* kvs_kernel the attend launches use */
+  int32_t attend_grid;       /* CTAs of one tensor-core attend launch (persistent) */
+  int32_t reserved[2];
+} kvs_layout;
+
+KVS_API kvs_status kvs_get_layout(const kvs_ctx* ctx, kvs_layout* out);
+
+/* Synchronise `stream` and report the device error word (KVS_OK if clear). */
+KVS_API kvs_status kvs_get_status(kvs_ctx* ctx, kvs_stream_t stream);
+
+/* Clear the device error word and the attend arrival counters (after a timeout). */
+KVS_API kvs_status kvs_clear_error(kvs_ctx* ctx, kvs_stream_t stream);
+
+/* Message of the last failed call on ctx ("" if none); never NULL. */
+KVS_API const char* kvs_last_error(const kvs_ctx* ctx);
+
+KVS_API const char* kvs_status_string(kvs_status s);
+
+KVS_API int32_t kvs_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVS_H */

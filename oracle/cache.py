@@ -110,8 +110,9 @@ class OracleKV:
             self.v_vals = np.zeros(shape, dtype=np.float32)
         self.resident_blocks = [set() for _ in range(num_seqs)]      # H2O mode only
         self.scores = [ScoreTables(max_positions, block_tokens, ema_decay) for _ in range(num_seqs)]
-        self._tok_mass = {}      # (l, b) -> (positions, token mass) of the current step
-        self._blk_mass = {}      # (l, b) -> {block: mass} of the current step
+        self._tok_mass = {}      # (l, b) -> (positions, token mass) of the latest attend
+        self._blk_mass = {}      # (l, b) -> {block: mass} of the latest attend
+        self._attended = set()   # (l, b) attended since the last accumulate
 
     # ---------------------------------------------------------------- a1 append
     def append(self, layer, seq, k, v):
@@ -175,6 +176,7 @@ class OracleKV:
         out, w = attention.decode_attention(q, k, v)
         self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(w))
         self._blk_mass[(layer, seq)] = attention.block_step_mass(w, pos, self.block)
+        self._attended.add((layer, seq))
         return out, w, pos
 
     def token_mass(self, layer, seq):
@@ -199,11 +201,12 @@ class OracleKV:
             x_tok = np.zeros(n)
             y_blk = np.zeros(-(-n // self.block))
             for l in range(self.L):
-                if (l, b) not in self._tok_mass:
+                if (l, b) not in self._attended:
                     raise ValueError("layer %d of sequence %d was not attended this step" % (l, b))
-                pos, tau = self._tok_mass.pop((l, b))
+                self._attended.discard((l, b))
+                pos, tau = self._tok_mass[(l, b)]
                 x_tok[pos] += tau                      # sum over layers
-                for k, m in self._blk_mass.pop((l, b)).items():
+                for k, m in self._blk_mass[(l, b)].items():
                     y_blk[k] = max(y_blk[k], m)        # max over layers
             self.scores[b].update(n, x_tok, y_blk)
             result[b] = (x_tok, y_blk)

@@ -1,0 +1,184 @@
+"""GPU parity: the CUDA path through the C ABI against the float64 oracle.
+
+Sizes are small enough for the oracle to follow every sequence and every step, yet
+span several 16-token blocks, several CTAs per sequence and ragged tails.  Bars:
+E4M3 codes, scales, slots and absolute positions bit-exact; attention output within
+2e-3 (bf16 / E4M3 inputs) or 1e-4 (f32) max relative error per (sequence, head) row;
+masses and score tables within 1e-4 absolute; kept block sets equal except for
+blocks whose oracle score lies within 1e-4 of the cut-off.
+"""
+import numpy as np
+import pytest
+import torch
+
+import attention_scored_kv_gb300 as kvs
+import workloads
+from tests import harness
+
+pytestmark = pytest.mark.gpu
+
+
+def _full_check(wl, kernel=kvs.KERNEL_AUTO, steps=None, every=1):
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kernel)
+    run.prefill()
+    worst = 0.0
+    n = wl.steps if steps is None else steps
+    for t in range(n):
+        res = run.decode_step(select=False)
+        worst = max(worst, res["out_err"])
+        check = t % every == 0 or t == n - 1
+        if check:   # masses are read through the block table, so before any eviction
+            harness.check_masses(run)
+            harness.check_scores(run)
+        keep = run.select()
+        if check:
+            harness.check_selection(run, keep)
+    harness.check_storage(run)
+    assert worst <= harness.OUT_TOL[wl.kv_format], worst
+    assert run.cache.get_status() == 0, run.cache.last_error()
+    return run, worst
+
+
+# ------------------------------------------------------------------ tiny (general kernel)
+@pytest.mark.parametrize("seed", [7, 19, 41])
+def test_tiny_f32_window4(seed):
+    wl = workloads.scaled_down("tiny-f32-window4", name="tiny-%d" % seed, seed=seed)
+    run, _ = _full_check(wl)
+    assert run.cache.layout().attend_kernel == kvs.KERNEL_GENERAL
+
+
+# ------------------------------------------------------------------ tensor-core kernel
+SMALL = {
+    "bf16": workloads.scaled_down("bf16-b8-ctx4096", num_layers=2, batch=3, context=300, steps=12),
+    "e4m3-window": workloads.scaled_down("e4m3-b16-ctx32768-window4096", num_layers=2, batch=3, context=700,
+                                         window=256, steps=12, prefill_chunk=128),
+    "e4m3-nowindow": workloads.scaled_down("e4m3-b16-ctx32768-window4096", num_layers=2, batch=2, context=513,
+                                           window=0, steps=6, prefill_chunk=0),
+    "bf16-hkv8": workloads.scaled_down("bf16-b1-ctx131072-planted", num_layers=2, batch=2, context=1000,
+                                       retrieval_pos=500, steps=6, prefill_chunk=0),
+    "e4m3-h2o": workloads.scaled_down("e4m3-b64-ragged-h2o2048", num_layers=2, batch=5, context_range=(100, 700),
+                                      h2o_budget_tokens=256, steps=40, prefill_chunk=256),
+}
+
+
+@pytest.mark.parametrize("name", sorted(SMALL))
+def test_tensor_kernel_small(name):
+    wl = SMALL[name]
+    run, worst = _full_check(wl, kernel=kvs.KERNEL_TENSOR, every=3)
+    assert run.cache.layout().attend_kernel == kvs.KERNEL_TENSOR
+
+
+@pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-h2o"])
+def test_general_kernel_on_tensor_shapes(name):
+    wl = SMALL[name]
+    wl = workloads.scaled_down(wl.name.replace("-small", ""), **{**_fields(wl), "steps": 6})
+    run, _ = _full_check(wl, kernel=kvs.KERNEL_GENERAL, every=2)
+    assert run.cache.layout().attend_kernel == kvs.KERNEL_GENERAL
+
+
+def _fields(wl):
+    import dataclasses
+    d = dataclasses.asdict(wl)
+    d.pop("name")
+    return d
+
+
+def test_tensor_and_general_agree():
+    wl = SMALL["e4m3-window"]
+    outs = []
+    for kern in (kvs.KERNEL_TENSOR, kvs.KERNEL_GENERAL):
+        run = harness.Run(wl, oracle_seqs=[], kernel=kern)
+        run.prefill()
+        for _ in range(3):
+            run.decode_step(select=False)
+        outs.append(torch.stack([run.last_out[l] for l in range(wl.num_layers)]).double().cpu().numpy())
+    assert harness.rel_err_rows(outs[0], outs[1]) <= 2e-3
+
+
+# ------------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("window,context,kernel", [
+    (1, 5, kvs.KERNEL_GENERAL),          # window 1: only the token just written
+    (4, 1, kvs.KERNEL_GENERAL),          # a single prefilled token
+    (20, 57, kvs.KERNEL_GENERAL),        # window not a multiple of 16: blocks straddle pages
+    (16, 33, kvs.KERNEL_TENSOR),         # one page per sequence, wraps every 16 steps
+    (32, 0, kvs.KERNEL_TENSOR),          # empty prefill: decode from the first token
+])
+def test_window_edges(window, context, kernel):
+    base = "tiny-f32-window4" if kernel == kvs.KERNEL_GENERAL else "e4m3-b16-ctx32768-window4096"
+    ch = dict(window=window, context=context, steps=20, prefill_chunk=7 if context else 0)
+    if kernel == kvs.KERNEL_TENSOR:
+        ch.update(num_layers=2, batch=2)
+    wl = workloads.scaled_down(base, name="edge-w%d-c%d" % (window, context), **ch)
+    _full_check(wl, kernel=kernel)
+
+
+def test_prefill_chunk_longer_than_window():
+    wl = workloads.scaled_down("e4m3-b16-ctx32768-window4096", name="chunk-gt-window", num_layers=1, batch=2,
+                               context=300, window=64, steps=3, prefill_chunk=200)
+    _full_check(wl, kernel=kvs.KERNEL_TENSOR)
+
+
+def test_many_sequences_per_cta():
+    # 200 short sequences: several sequence boundaries inside one CTA's share
+    wl = workloads.scaled_down("e4m3-b16-ctx32768-window4096", name="many-seqs", num_layers=1, batch=200,
+                               context=20, window=0, steps=2, prefill_chunk=0)
+    run = harness.Run(wl, oracle_seqs=[0, 1, 99, 199], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    for _ in range(wl.steps):
+        res = run.decode_step()
+        assert res["out_err"] <= 2e-3
+        harness.check_masses(run)
+        harness.check_scores(run)
+    assert run.cache.get_status() == 0
+
+
+# ------------------------------------------------------------------ errors
+def test_attend_on_empty_cache_is_rejected():
+    wl = SMALL["bf16"]
+    c = kvs.KVCache(harness.make_config(wl))
+    q = torch.zeros((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kvs.KVSError) as e:
+        c.decode_attend(0, q)
+    assert e.value.status == 3
+
+
+def test_capacity_is_enforced():
+    wl = workloads.scaled_down("bf16-b8-ctx4096", num_layers=1, batch=1, context=0, steps=4)
+    c = kvs.KVCache(harness.make_config(wl))
+    k = torch.zeros((1, 5, wl.num_kv_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(kvs.KVSError) as e:
+        c.append_kv(0, k, k)
+    assert e.value.status == 2
+    # a failed call leaves the state unchanged
+    assert harness.StateView(c, wl).next_position(0)[0] == 0
+
+
+def test_eviction_needs_h2o_mode():
+    wl = SMALL["bf16"]
+    c = kvs.KVCache(harness.make_config(wl))
+    with pytest.raises(kvs.KVSError) as e:
+        c.select_blocks(4, flags=kvs.SELECT_APPLY)
+    assert e.value.status == 1
+
+
+def test_layers_must_agree_at_accumulate():
+    wl = workloads.scaled_down("bf16-b8-ctx4096", num_layers=2, batch=1, context=0, steps=4)
+    c = kvs.KVCache(harness.make_config(wl))
+    k = torch.zeros((1, 1, wl.num_kv_heads, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    c.append_kv(0, k, k)
+    with pytest.raises(kvs.KVSError) as e:
+        c.accumulate_scores()
+    assert e.value.status == 7
+
+
+def test_bounded_wait_reports_timeout_and_recovers():
+    """spin_limit -1: a CTA that is not the last of its sequence to arrive gives up at
+    once and flags KVS_ERR_TIMEOUT; the context is usable again after clear_error."""
+    wl = workloads.scaled_down("e4m3-b16-ctx32768-window4096", name="timeout", num_layers=1, batch=1,
+                               context=4096, window=0, steps=1, prefill_chunk=0)
+    run = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR, spin_limit=-1)
+    run.prefill()
+    run.decode_step(select=False)
+    assert run.cache.get_status() == 5          # KVS_ERR_TIMEOUT
+    run.cache.clear_error()
+    assert run.cache.get_status() == 0

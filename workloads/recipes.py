@@ -102,9 +102,9 @@ def get(name):
     return WORKLOADS[name]
 
 
-def scaled_down(name, **changes):
+def scaled_down(base_name, **changes):
     """A smaller copy of a named workload (same structure, other sizes)."""
-    base = WORKLOADS[name]
+    base = WORKLOADS[base_name]
     return dataclasses.replace(base, name=changes.pop("name", base.name + "-small"), **changes)
 
 
