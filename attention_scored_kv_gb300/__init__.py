@@ -139,6 +139,19 @@ class KVCache:
                                             _stream(stream)))
         return out
 
+    def decode_attend_static_scratch(self, layer, q, out=None, seq_begin=0, stream=None):
+        """decode_attend with the exchange area in the library's own fixed array instead
+        of this cache's workspace (for callers that cannot supply device memory)."""
+        _, Hq, _, D = self.shape
+        n_seqs = int(q.shape[0])
+        _need(q, "q", self.in_dtype, (n_seqs, Hq, D))
+        if out is None:
+            out = torch.empty((n_seqs, Hq, D), dtype=torch.float32, device=q.device)
+        _need(out, "out", torch.float32, (n_seqs, Hq, D))
+        self._check(lib().kvs_decode_attend_static_scratch(self._ctx, layer, seq_begin, n_seqs, _ptr(q), _ptr(out),
+                                                           _stream(stream)))
+        return out
+
     def accumulate_scores(self, seq_begin=0, n_seqs=None, stream=None):
         n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
         self._check(lib().kvs_accumulate_scores(self._ctx, seq_begin, n, _stream(stream)))

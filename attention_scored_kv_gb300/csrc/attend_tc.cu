@@ -692,4 +692,84 @@ int tc_grid(int kv_dtype, int Hkv, int sm_count) {
   return g > kGridMax ? kGridMax : g;
 }
 
+// ----------------------------------------------------------------------------------
+// Tensor-core attend with its exchange area in a library-owned array.
+//
+// The attend launch needs an exchange area: one (m, l, o) record per CTA and sequence
+// and two arrival counters per sequence.  kvs_decode_attend takes it from the caller's
+// workspace; this variant takes it from the array below, compiled into the library, so
+// a call asks the caller for nothing but its inputs and outputs.  The array holds
+// kStaticScratchBytes; a launch that needs more is refused.  Every call (every context,
+// every stream) shares it and it keeps the last call's contents: the counters are
+// cleared on the call's stream before each launch, and two such launches that overlap
+// on the GPU race on it.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;
+static __device__ __align__(256) unsigned char g_attend_scratch[kStaticScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+void* g_scratch_addr[kMaxDevices] = {};
+}  // namespace
+
+size_t static_scratch_limit() { return kStaticScratchBytes; }
+
+// Bytes of the array one launch uses: records for CTA + sequence index < grid + n_seqs,
+// then 2 * max_seqs counters (indexed by absolute sequence).
+size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* counters_offset) {
+  const size_t rec = (size_t)(grid + n_seqs) * d.Hq * (kD + 2) * sizeof(float);
+  const size_t off = (rec + 255) & ~size_t(255);
+  *counters_offset = off;
+  return off + 2 * (size_t)d.max_seqs * sizeof(int32_t);
+}
+
+// Device address of the array on the current device, looked up once per device (the
+// host-side symbol is only a stand-in, never a device address).
+cudaError_t static_scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attend_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+// Returns cudaErrorInvalidValue if the launch needs more than the array holds and
+// cudaErrorNotSupported if its logits do not fit in shared memory (that case needs the
+// workspace's logit scratch).
+cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
+                                    int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
+                                    int grid, cudaStream_t st) {
+  size_t counters_off = 0;
+  if (static_scratch_need(d, n_seqs, grid, &counters_off) > kStaticScratchBytes) return cudaErrorInvalidValue;
+  Params P;
+  P.layer = layer;
+  P.seq_begin = seq_begin;
+  P.n_seqs = n_seqs;
+  P.cap = tc_cap(T_bound, grid);
+  if (P.cap < 1) P.cap = 1;
+  P.q = q;
+  P.out = out;
+  P.qk_scale = kLog2e / sqrtf((float)kD);
+  const bool fp8 = d.kv_dtype == KVS_E4M3;
+  const size_t need_smem = d.Hkv == 4 ? (fp8 ? smem_bytes<4, true, true>(P.cap, n_seqs) : smem_bytes<4, false, true>(P.cap, n_seqs))
+                                      : (fp8 ? smem_bytes<8, true, true>(P.cap, n_seqs) : smem_bytes<8, false, true>(P.cap, n_seqs));
+  if (need_smem > tc_smem_limit()) return cudaErrorNotSupported;
+  void* base = nullptr;
+  cudaError_t e = static_scratch_address(&base);
+  if (e != cudaSuccess) return e;
+  Dev dd = d;
+  dd.partials = static_cast<float*>(base);
+  dd.counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + counters_off);
+  e = cudaMemsetAsync(dd.counters, 0, 2 * (size_t)d.max_seqs * sizeof(int32_t), st);
+  if (e != cudaSuccess) return e;
+  if (d.Hkv == 4) return fp8 ? launch_one<4, true, true>(tk, tv, dd, P, grid, st) : launch_one<4, false, true>(tk, tv, dd, P, grid, st);
+  return fp8 ? launch_one<8, true, true>(tk, tv, dd, P, grid, st) : launch_one<8, false, true>(tk, tv, dd, P, grid, st);
+}
+
 }  // namespace kvs

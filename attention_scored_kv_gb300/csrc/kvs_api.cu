@@ -24,6 +24,11 @@ cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
                              int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound, int grid,
                              cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
+size_t static_scratch_limit();
+size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* counters_offset);
+cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
+                                    int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
+                                    int grid, cudaStream_t st);
 }  // namespace kvs
 
 using namespace kvs;
@@ -405,6 +410,35 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
                    "tensor-core attend");
   }
   return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
+}
+
+kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                                            const void* d_q, float* d_out, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if (ctx->kernel != KVS_KERNEL_TENSOR)
+    return fail(ctx, KVS_ERR_UNSUPPORTED, "the library-owned exchange area serves the tensor-core attend only");
+  const int B = ctx->cfg.max_seqs;
+  int64_t T_bound = 0;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    if (ctx->next[(size_t)layer * B + s] == 0)
+      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
+    T_bound += seq_block_bound(ctx, s);
+  }
+  size_t off = 0;
+  const size_t need = static_scratch_need(ctx->dev, n_seqs, ctx->grid, &off);
+  if (need > static_scratch_limit())
+    return fail(ctx, KVS_ERR_CAPACITY, "this launch needs %zu bytes of exchange area; the library array holds %zu",
+                need, static_scratch_limit());
+  const cudaError_t e = launch_attend_tc_static(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
+                                                seq_begin, n_seqs, d_q, d_out, T_bound, ctx->grid,
+                                                reinterpret_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported)
+    return fail(ctx, KVS_ERR_UNSUPPORTED, "the logits of this launch do not fit in shared memory");
+  return cuda_ok(ctx, e, "tensor-core attend (library exchange area)");
 }
 
 kvs_status kvs_accumulate_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream) {

@@ -163,6 +163,36 @@ KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
 KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
                              const void* d_q, float* d_out, kvs_stream_t stream);
 
+/* kvs_decode_attend without any exchange area from the caller.  No page counterpart:
+ * this is a deployment variant, not a step of the method.
+ *
+ * The tensor-core attend needs a per-launch exchange area (one softmax partial per
+ * CTA and sequence, two arrival counters per sequence).  kvs_decode_attend keeps it in
+ * the context's workspace.  This entry point instead uses one fixed array of 8 MiB
+ * compiled into the library (a __device__ array each GPU that loads the library holds
+ * until the process exits), so the call itself needs no device memory beyond the
+ * cache it reads and the q / out buffers it is given.  It is for callers that cannot
+ * obtain device memory when they run a decode step: a runtime whose device memory is
+ * parcelled out once at start-up by a supervisor, code that must not enter the CUDA
+ * allocator (which can synchronise the device and fail under memory pressure), or a
+ * caller that wants to hand the library nothing but its inputs and outputs.
+ *
+ * Same arguments, same results and same errors as kvs_decode_attend, plus:
+ *   KVS_ERR_UNSUPPORTED  the context does not use the tensor-core attend, or this
+ *                        launch's logits do not fit in shared memory;
+ *   KVS_ERR_CAPACITY     the launch needs more than the array holds:
+ *                        (grid + n_seqs) * num_q_heads * (head_dim + 2) * 4 bytes,
+ *                        rounded up to 256, plus 8 * max_seqs bytes must be <= 8 MiB.
+ * The array is shared by every call of every context on the device and keeps the last
+ * call's contents; the counters are cleared on `stream` before each launch.  Two such
+ * launches that overlap on the GPU (different streams or contexts) race on the array:
+ * order them.  The first call on a device looks up the array's device address (a
+ * host-side API call, done once per device); make that first call before any stream
+ * capture. */
+KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
+                                                    int32_t n_seqs, const void* d_q, float* d_out,
+                                                    kvs_stream_t stream);
+
 /* Fold this step's masses of every layer into the score tables of the range:
  * token score x_p = sum over layers of the entry masses, block score y_k = max over
  * layers of the block masses; for every tracked entry (every position below
