@@ -20,6 +20,16 @@ namespace {
 
 constexpr int kBlocksPerCta = 16;     // 16 blocks x 16 positions = 256 threads
 
+// EMA value as of step `step - 1` of an entry last written at step `last` (-1: never).
+// An entry resident in the previous step (the common case) needs no power at all.
+__device__ __forceinline__ double decayed(double e, int32_t last, int32_t step, double dec) {
+  if (last < 0) return 0.0;
+  const int32_t gap = step - 1 - last;
+  if (gap == 0) return e;
+  if (gap == 1) return e * dec;
+  return e * pow(dec, (double)gap);
+}
+
 __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
   const int s = seq_begin + blockIdx.y;
   const SeqBlocks sb = seq_blocks(d, 0, s);
@@ -39,7 +49,7 @@ __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
         x += (double)d.tok_mass[(size_t)l * d.slot_layer_elems + (size_t)page * kBlock + slot];
       const size_t t = (size_t)s * d.max_positions + p;
       const int32_t last = d.last_tok[t];
-      const double e_prev = (last < 0) ? 0.0 : d.e_tok[t] * pow(dec, (double)(step - 1 - last));
+      const double e_prev = decayed(d.e_tok[t], last, step, dec);
       d.c_tok[t] += x;
       d.e_tok[t] = dec * e_prev + (1.0 - dec) * x;
       d.last_tok[t] = step;
@@ -50,7 +60,7 @@ __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
         y = fmaxf(y, d.blk_mass[(size_t)l * d.blk_layer_elems + (size_t)s * d.max_blocks + k]);
       const size_t t = (size_t)s * d.max_blocks + k;
       const int32_t last = d.last_blk[t];
-      const double e_prev = (last < 0) ? 0.0 : d.e_blk[t] * pow(dec, (double)(step - 1 - last));
+      const double e_prev = decayed(d.e_blk[t], last, step, dec);
       d.c_blk[t] += (double)y;
       d.e_blk[t] = dec * e_prev + (1.0 - dec) * (double)y;
       d.last_blk[t] = step;

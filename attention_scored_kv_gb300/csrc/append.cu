@@ -89,7 +89,7 @@ __device__ void store_position(const Dev& d, const void* src, size_t src_elem, u
   }
 }
 
-// grid (ceil(n_new / kWarps), n_seqs), one warp per new token.
+// grid (ceil(n_new / (kWarps/2)), n_seqs): two warps per new token, one for K, one for V.
 template <int KV, int IN>
 __global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, int seq_begin, int n_new,
                                                                const void* k_in, const void* v_in) {
@@ -98,7 +98,8 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, i
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t np_idx = (size_t)layer * d.max_seqs + s;
   const int64_t next0 = d.next_pos[np_idx];
-  const int i = blockIdx.x * kWarps + warp;
+  const int i = blockIdx.x * (kWarps / 2) + (warp >> 1);   // token; warp pairs split K and V
+  const bool is_k = (warp & 1) == 0;
   if (i < n_new) {
     const int64_t p = next0 + i;
     if (p >= d.max_positions) {
@@ -116,9 +117,12 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, i
         const size_t lay_slot = (size_t)layer * d.slot_layer_elems + (size_t)page * kBlock;
         uint8_t* kp = d.k_pages + layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
         uint8_t* vp = d.v_pages + layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
-        store_position<KV, IN>(d, k_in, src_elem, kp, d.k_scales ? d.k_scales + lay_slot + slot : nullptr, slot, lane);
-        store_position<KV, IN>(d, v_in, src_elem, vp, d.v_scales ? d.v_scales + lay_slot + slot : nullptr, slot, lane);
-        if (lane == 0) d.pos[lay_slot + slot] = p;
+        if (is_k) {
+          store_position<KV, IN>(d, k_in, src_elem, kp, d.k_scales ? d.k_scales + lay_slot + slot : nullptr, slot, lane);
+          if (lane == 0) d.pos[lay_slot + slot] = p;
+        } else {
+          store_position<KV, IN>(d, v_in, src_elem, vp, d.v_scales ? d.v_scales + lay_slot + slot : nullptr, slot, lane);
+        }
       }
     }
   }
@@ -175,7 +179,7 @@ cudaError_t launch_alloc_pages(const Dev& d, int layer, int seq_begin, int n_seq
 
 cudaError_t launch_append(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
                           const void* k, const void* v, cudaStream_t st) {
-  dim3 grid((n_new + kWarps - 1) / kWarps, n_seqs);
+  dim3 grid((n_new + kWarps / 2 - 1) / (kWarps / 2), n_seqs);
   const int KV = d.kv_dtype, IN = d.in_dtype;
   if (KV == KVS_E4M3 && IN == KVS_BF16) append_kernel<KVS_E4M3, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
   else if (KV == KVS_E4M3 && IN == KVS_F32) append_kernel<KVS_E4M3, KVS_F32><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);

@@ -15,8 +15,9 @@
 //     so a ragged batch balances by construction; a CTA's share is cut into segments
 //     (runs of blocks of one sequence).
 //   * One producer warp streams each block's K (then V) for all KV heads into a ring
-//     of shared-memory stages with TMA tensor copies (128-byte swizzle, L2 evict-first)
-//     completed on mbarriers; E4M3 scales arrive by bulk copy on the same barrier.
+//     of shared-memory stages (up to 128 KB, as deep as the free shared memory allows)
+//     with TMA tensor copies (128-byte swizzle, L2 evict-first) completed on mbarriers;
+//     E4M3 scales arrive by bulk copy on the same barrier.
 //   * Eight consumer warps, each bound to one KV head, run QK^T and PV on the tensor
 //     cores with mma.sync m16n8k16 (positions on M, the 8 heads of the group on N for
 //     QK^T; dimensions on M for PV).  E4M3 codes are decoded to f16 in registers
@@ -55,8 +56,9 @@ struct Cfg {
   static constexpr int HQ = HKV * kG;
   static constexpr int WPK = kNCW / HKV;                   // consumer warps per KV head
   static constexpr int ESZ = FP8 ? 1 : 2;
-  static constexpr int STAGE = HKV * kBlock * kD * ESZ;     // one block of K or V, all heads
-  static constexpr int NS = FP8 ? (HKV == 4 ? 10 : 6) : (HKV == 4 ? 6 : 4);
+  static constexpr int BLK = HKV * kBlock * kD * ESZ;       // one block of K or V, all heads
+  static constexpr int SB = 32768 / BLK;                    // blocks per ring stage (32 KB)
+  static constexpr int STAGE = SB * BLK;
   static constexpr int HALF = HKV * kBlock * 128;           // bf16: bytes of one 64-dim half
 };
 
@@ -155,38 +157,242 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t q, int64_t r) {
   return (int)(x < big ? x / (q + 1) : r + (x - big) / q);
 }
 
+// QK^T of NB (1 or 2) blocks of one ring stage for one KV head, interleaved for ILP:
+// logits (log2 domain, masked to -inf outside [lo, nxt)) go to the store, the running
+// per-head max is updated.  Block b sits in stage slot j0 + b*WPK, CTA-local block
+// index i_first + b*WPK.
+template <int HKV, bool FP8, int NB>
+__device__ __forceinline__ void qk_blocks(const uint8_t* stage, const float* sscale_st, int j0, int i_first,
+                                          const int32_t* blk_id, const uint32_t (&qf)[8][2], float* lg, int kvh,
+                                          int lane, int64_t lo, int64_t nxt, float qk_scale, float& mx0, float& mx1) {
+  using C = Cfg<HKV, FP8>;
+  constexpr int HQ = C::HQ, WPK = C::WPK;
+  const int g = lane >> 2, t = lane & 3;
+  float acc[NB][2][4];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) acc[b][c2][0] = acc[b][c2][1] = acc[b][c2][2] = acc[b][c2][3] = 0.f;
+  if constexpr (FP8) {
+    uint32_t w0[NB][8], w1[NB][8];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const uint8_t* kb = stage + (size_t)(j0 + b * WPK) * C::BLK + kvh * kBlock * kD;
+      const uint4 r0a = lds128(kb + g * kD + (((2 * t) ^ g) << 4));
+      const uint4 r0b = lds128(kb + g * kD + (((2 * t + 1) ^ g) << 4));
+      const uint4 r1a = lds128(kb + (g + 8) * kD + (((2 * t) ^ g) << 4));
+      const uint4 r1b = lds128(kb + (g + 8) * kD + (((2 * t + 1) ^ g) << 4));
+      w0[b][0] = r0a.x; w0[b][1] = r0a.y; w0[b][2] = r0a.z; w0[b][3] = r0a.w;
+      w0[b][4] = r0b.x; w0[b][5] = r0b.y; w0[b][6] = r0b.z; w0[b][7] = r0b.w;
+      w1[b][0] = r1a.x; w1[b][1] = r1a.y; w1[b][2] = r1a.z; w1[b][3] = r1a.w;
+      w1[b][4] = r1b.x; w1[b][5] = r1b.y; w1[b][6] = r1b.z; w1[b][7] = r1b.w;
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        mma_f16(acc[b][ks & 1], e4m3x2_to_f16x2(w0[b][ks] & 0xffffu), e4m3x2_to_f16x2(w1[b][ks] & 0xffffu),
+                e4m3x2_to_f16x2(w0[b][ks] >> 16), e4m3x2_to_f16x2(w1[b][ks] >> 16), qf[ks][0], qf[ks][1]);
+  } else {
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int half = ks >> 2, c0 = (2 * ks) & 7;
+      const int m = lane >> 3, row = ((m & 1) << 3) + (lane & 7), chunk = c0 + (m >> 1);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint8_t* base = stage + (size_t)(j0 + b * WPK) * C::BLK + half * C::HALF + kvh * kBlock * 128;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4(smem_u32(base + row * 128 + ((chunk ^ (row & 7)) << 4)), a0, a1, a2, a3);
+        mma_bf16(acc[b][ks & 1], a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int i = i_first + b * WPK;
+    const int64_t p0 = (int64_t)blk_id[i] * kBlock;
+    float sc0 = qk_scale, sc1 = qk_scale;
+    if constexpr (FP8) {
+      const float* sk = sscale_st + (j0 + b * WPK) * kBlock;
+      sc0 *= sk[g];
+      sc1 *= sk[g + 8];
+    }
+    float s00 = (acc[b][0][0] + acc[b][1][0]) * sc0, s01 = (acc[b][0][1] + acc[b][1][1]) * sc0;
+    float s10 = (acc[b][0][2] + acc[b][1][2]) * sc1, s11 = (acc[b][0][3] + acc[b][1][3]) * sc1;
+    if (p0 < lo || p0 + kBlock > nxt) {                 // a block the window or the end cuts
+      if (!(p0 + g >= lo && p0 + g < nxt)) s00 = s01 = -INFINITY;
+      if (!(p0 + g + 8 >= lo && p0 + g + 8 < nxt)) s10 = s11 = -INFINITY;
+    }
+    const int h0 = kvh * kG + 2 * t;
+    lg[lidx<HQ>(i, h0, g)] = s00;
+    lg[lidx<HQ>(i, h0 + 1, g)] = s01;
+    lg[lidx<HQ>(i, h0, g + 8)] = s10;
+    lg[lidx<HQ>(i, h0 + 1, g + 8)] = s11;
+    mx0 = fmaxf(mx0, fmaxf(s00, s10));
+    mx1 = fmaxf(mx1, fmaxf(s01, s11));
+  }
+}
+
+// PV of NB (1 or 2) blocks of one ring stage for one KV head: p = exp2(s - m) written
+// back over the logits, per-head in-block sums to bsum, the running l, and the MMAs
+// into the shared accumulators o (dimensions on M, heads on N).
+template <int HKV, bool FP8, int NB>
+__device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* sscale_st, int j0, int i_first, float* lg,
+                                          float* bsum, int kvh, int lane, float mh, float& lsum, float (&o)[8][4]) {
+  using C = Cfg<HKV, FP8>;
+  constexpr int HQ = C::HQ, WPK = C::WPK;
+  const int g = lane >> 2, t = lane & 3;
+  const int hg = kvh * kG + g;
+  float p[NB][4];
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int i = i_first + b * WPK;
+    float2* pa = reinterpret_cast<float2*>(lg + lidx<HQ>(i, hg, 2 * t));
+    float2* pb = reinterpret_cast<float2*>(lg + lidx<HQ>(i, hg, 2 * t + 8));
+    const float2 sa = *pa, sbv = *pb;
+    p[b][0] = exp2f(sa.x - mh);
+    p[b][1] = exp2f(sa.y - mh);
+    p[b][2] = exp2f(sbv.x - mh);
+    p[b][3] = exp2f(sbv.y - mh);
+    float bpart = (p[b][0] + p[b][1]) + (p[b][2] + p[b][3]);   // this thread's share of the block
+    lsum += bpart;
+    *pa = make_float2(p[b][0], p[b][1]);
+    *pb = make_float2(p[b][2], p[b][3]);
+    bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
+    bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
+    if (t == 0) bsum[i * HQ + hg] = bpart;
+  }
+  if constexpr (FP8) {
+    uint32_t b0[NB], b1[NB];
+    uint32_t x0[NB][4], y0[NB][4], x2[NB][4], y2[NB][4];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float* sv = sscale_st + (j0 + b * WPK) * kBlock;
+      b0[b] = pack_f16(p[b][0] * sv[2 * t] * kVFold, p[b][1] * sv[2 * t + 1] * kVFold);
+      b1[b] = pack_f16(p[b][2] * sv[2 * t + 8] * kVFold, p[b][3] * sv[2 * t + 9] * kVFold);
+      const uint8_t* vb = stage + (size_t)(j0 + b * WPK) * C::BLK + kvh * kBlock * kD;
+      const uint4 L0 = lds128(vb + (2 * t) * kD + ((g ^ (2 * t)) << 4));
+      const uint4 L1 = lds128(vb + (2 * t + 1) * kD + ((g ^ (2 * t + 1)) << 4));
+      const uint4 L2 = lds128(vb + (2 * t + 8) * kD + ((g ^ (2 * t)) << 4));
+      const uint4 L3 = lds128(vb + (2 * t + 9) * kD + ((g ^ (2 * t + 1)) << 4));
+      x0[b][0] = L0.x; x0[b][1] = L0.y; x0[b][2] = L0.z; x0[b][3] = L0.w;
+      y0[b][0] = L1.x; y0[b][1] = L1.y; y0[b][2] = L1.z; y0[b][3] = L1.w;
+      x2[b][0] = L2.x; x2[b][1] = L2.y; x2[b][2] = L2.z; x2[b][3] = L2.w;
+      y2[b][0] = L3.x; y2[b][1] = L3.y; y2[b][2] = L3.z; y2[b][3] = L3.w;
+    }
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint32_t lo = prmt(x0[b][w], y0[b][w], 0x5140), hi = prmt(x0[b][w], y0[b][w], 0x7362);
+        const uint32_t lo2 = prmt(x2[b][w], y2[b][w], 0x5140), hi2 = prmt(x2[b][w], y2[b][w], 0x7362);
+        mma_f16(o[2 * w], e4m3x2_to_f16x2(lo & 0xffffu), e4m3x2_to_f16x2(lo >> 16),
+                e4m3x2_to_f16x2(lo2 & 0xffffu), e4m3x2_to_f16x2(lo2 >> 16), b0[b], b1[b]);
+        mma_f16(o[2 * w + 1], e4m3x2_to_f16x2(hi & 0xffffu), e4m3x2_to_f16x2(hi >> 16),
+                e4m3x2_to_f16x2(hi2 & 0xffffu), e4m3x2_to_f16x2(hi2 >> 16), b0[b], b1[b]);
+      }
+  } else {
+    uint32_t bh0[NB], bh1[NB], bl0[NB], bl1[NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      const float h0 = __bfloat162float(__float2bfloat16_rn(p[b][0])), h1 = __bfloat162float(__float2bfloat16_rn(p[b][1]));
+      const float h8 = __bfloat162float(__float2bfloat16_rn(p[b][2])), h9 = __bfloat162float(__float2bfloat16_rn(p[b][3]));
+      bh0[b] = pack_bf16(h0, h1);
+      bh1[b] = pack_bf16(h8, h9);
+      bl0[b] = pack_bf16(p[b][0] - h0, p[b][1] - h1);
+      bl1[b] = pack_bf16(p[b][2] - h8, p[b][3] - h9);
+    }
+#pragma unroll
+    for (int mb = 0; mb < 8; ++mb) {
+      const int half = mb >> 2, c0 = (2 * mb) & 7;
+      const int m = lane >> 3, pos = ((m >> 1) << 3) + (lane & 7), chunk = c0 + (m & 1);
+#pragma unroll
+      for (int b = 0; b < NB; ++b) {
+        const uint8_t* base = stage + (size_t)(j0 + b * WPK) * C::BLK + half * C::HALF + kvh * kBlock * 128;
+        uint32_t a0, a1, a2, a3;
+        ldsm_x4_t(smem_u32(base + pos * 128 + ((chunk ^ (pos & 7)) << 4)), a0, a1, a2, a3);
+        mma_bf16(o[mb], a0, a1, a2, a3, bh0[b], bh1[b]);
+        mma_bf16(o[mb], a0, a1, a2, a3, bl0[b], bl1[b]);
+      }
+    }
+  }
+}
+
+constexpr int kSC = 32;                 // partial records per round of the normaliser
+constexpr int kRingBytes = 128 * 1024;  // shared memory given to the TMA ring at most
+constexpr int kMinStages = 2;
+constexpr int kStageBytes = 32768;      // a ring stage: each completion costs ~0.3 us, so
+                                        // stages are 32 KB (several 16-token blocks)
+
 struct Params {
   int layer, seq_begin, n_seqs, cap;   // cap: blocks per CTA the buffers hold
+  int ns;                              // ring stages
   const void* q;                       // [n_seqs][HQ][D] bf16
   float* out;                          // [n_seqs][HQ][D]
   float qk_scale;                      // log2(e) / sqrt(D)
 };
+
+// Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
+// so every stage keeps the 1024-byte alignment the 128-byte swizzle needs.
+struct SmemPlan {
+  size_t ring, sscale, bars, blk, prefix, mbuf, lbuf, hv, flag, pm, pl, bsum, obuf, lg, total;
+};
+
+__host__ __device__ inline size_t up16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int cap, int n_seqs, int ns) {
+  const int HQ = hkv * kG, WPK = kNCW / hkv;
+  const size_t blk = (size_t)hkv * kBlock * kD * (fp8 ? 1 : 2);
+  const size_t sb = kStageBytes / blk;
+  SmemPlan p;
+  size_t o = 0;
+  p.ring = o;   o += (size_t)ns * sb * blk;
+  p.sscale = o; o += (size_t)ns * sb * kBlock * 4;
+  p.bars = o;   o += (size_t)2 * ns * 8;
+  p.blk = o;    o = up16(o + (size_t)3 * cap * 4);
+  p.prefix = o; o = up16(o + (size_t)(n_seqs + 1) * 4);
+  p.mbuf = o;   o += (size_t)WPK * HQ * 4;
+  p.lbuf = o;   o += (size_t)WPK * HQ * 4;
+  p.hv = o;     o += (size_t)4 * HQ * 4;
+  p.flag = o;   o += 16;
+  p.pm = o;     o += (size_t)kSC * HQ * 4;
+  p.pl = o;     o += (size_t)kSC * HQ * 4;
+  p.bsum = o;   o = up16(o + (size_t)cap * HQ * 4);
+  p.obuf = o;   o += (WPK == 2 ? (size_t)hkv * 32 * 32 * 4 : 0);
+  p.lg = o;     o += lsmem ? (size_t)cap * HQ * kBlock * 4 : 0;
+  p.total = o + 1024;                       // alignment slack
+  return p;
+}
 
 template <int HKV, bool FP8, bool LSMEM>
 __global__ void __launch_bounds__(kThreads, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Dev d, const Params P) {
   using C = Cfg<HKV, FP8>;
-  constexpr int HQ = C::HQ, NS = C::NS, WPK = C::WPK, REC = kD + 2;
+  constexpr int HQ = C::HQ, WPK = C::WPK, REC = kD + 2;
+  const int NS = P.ns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring = smem;                                           // NS * STAGE
-  float* sscale = reinterpret_cast<float*>(ring + NS * C::STAGE); // NS * 16 (E4M3)
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sscale + NS * kBlock);   // full[NS], empty[NS]
-  int32_t* blk_id = reinterpret_cast<int32_t*>(bars + 2 * NS);
+  const SmemPlan sp = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, NS);
+  uint8_t* ring = smem + sp.ring;
+  float* sscale = reinterpret_cast<float*>(smem + sp.sscale);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.bars);          // full[NS], empty[NS]
+  int32_t* blk_id = reinterpret_cast<int32_t*>(smem + sp.blk);
   int32_t* blk_page = blk_id + P.cap;
   int32_t* blk_seq = blk_page + P.cap;
-  int32_t* prefix = blk_seq + P.cap;                              // [n_seqs + 1]
-  float* mbuf = reinterpret_cast<float*>(prefix + P.n_seqs + 1); // [WPK][HQ]
-  float* lbuf = mbuf + WPK * HQ;                                  // [WPK][HQ]
-  float* mseg = lbuf + WPK * HQ;                                  // [HQ]
-  float* cfac = mseg + HQ;                                        // [HQ]
-  float* gmax = cfac + HQ;                                        // [HQ]
-  float* ginv = gmax + HQ;                                        // [HQ]
-  int32_t* flag = reinterpret_cast<int32_t*>(ginv + HQ);          // [4]
-  float* obuf = reinterpret_cast<float*>(flag + 4);               // WPK==2: [HKV][32 regs][32 lanes]
-  float* lg_smem = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(obuf + (WPK == 2 ? HKV * 32 * 32 : 0)) + 15) & ~uintptr_t(15));
+  int32_t* prefix = reinterpret_cast<int32_t*>(smem + sp.prefix);       // [n_seqs + 1]
+  float* mbuf = reinterpret_cast<float*>(smem + sp.mbuf);              // [WPK][HQ]
+  float* lbuf = reinterpret_cast<float*>(smem + sp.lbuf);              // [WPK][HQ]
+  float* mseg = reinterpret_cast<float*>(smem + sp.hv);                // [HQ]
+  float* cfac = mseg + HQ;                                             // [HQ]
+  float* gmax = cfac + HQ;                                             // [HQ]
+  float* ginv = gmax + HQ;                                             // [HQ]
+  int32_t* flag = reinterpret_cast<int32_t*>(smem + sp.flag);
+  float* pm = reinterpret_cast<float*>(smem + sp.pm);                  // [kSC][HQ]
+  float* pl = reinterpret_cast<float*>(smem + sp.pl);                  // [kSC][HQ]
+  float* bsum = reinterpret_cast<float*>(smem + sp.bsum);              // [cap][HQ]
+  float* obuf = reinterpret_cast<float*>(smem + sp.obuf);              // WPK==2: [HKV][32][32]
+  float* lg_smem = reinterpret_cast<float*>(smem + sp.lg);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
@@ -238,7 +444,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, HKV);
+      mbar_init(empty0 + 8 * s, kNCW);      // every consumer warp releases every stage
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -264,19 +470,22 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         for (int ph = 0; ph < 2; ++ph) {
           const CUtensorMap* map = ph == 0 ? &tmk : &tmv;
           const float* scales = ph == 0 ? d.k_scales : d.v_scales;
-          for (int i = i0; i < i1; ++i, ++ctr) {
+          for (int g0 = i0; g0 < i1; g0 += C::SB, ++ctr) {      // one stage = up to SB blocks
+            const int nb = min(C::SB, i1 - g0);
             const uint32_t st = ctr % NS, round = ctr / NS;
             if (round > 0 && !mbar_wait(empty0 + 8 * st, (round - 1) & 1)) set_error(d, kErrTimeout);
             const uint32_t fb = full0 + 8 * st;
-            const uint32_t dst = smem_u32(ring + st * C::STAGE);
-            mbar_expect_tx(fb, C::STAGE + (FP8 ? kBlock * 4 : 0));
-            if constexpr (FP8) {
-              tma_load_4d(dst, map, 0, 0, 0, blk_page[i], fb, pol);
-              bulk_load(smem_u32(sscale + st * kBlock), scales + lay_slot + (size_t)blk_page[i] * kBlock,
-                        kBlock * 4, fb);
-            } else {
-              tma_load_4d(dst, map, 0, 0, 0, blk_page[i], fb, pol);
-              tma_load_4d(dst + C::HALF, map, 64, 0, 0, blk_page[i], fb, pol);
+            mbar_expect_tx(fb, nb * (C::BLK + (FP8 ? kBlock * 4 : 0)));
+            for (int j = 0; j < nb; ++j) {
+              const int page = blk_page[g0 + j];
+              const uint32_t dst = smem_u32(ring + (size_t)st * C::STAGE + (size_t)j * C::BLK);
+              tma_load_4d(dst, map, 0, 0, 0, page, fb, pol);
+              if constexpr (FP8) {
+                bulk_load(smem_u32(sscale + (st * C::SB + j) * kBlock), scales + lay_slot + (size_t)page * kBlock,
+                          kBlock * 4, fb);
+              } else {
+                tma_load_4d(dst + C::HALF, map, 64, 0, 0, page, fb, pol);
+              }
             }
           }
         }
@@ -317,54 +526,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 
       // ------------------------------------------------------------ pass 1: K
       float mx0 = -INFINITY, mx1 = -INFINITY;      // heads 2t, 2t+1 of this KV group
-      for (int i = i0; i < i1; ++i, ++ctr) {
-        if ((i & (WPK - 1)) != sub) continue;
+      for (int g0 = i0; g0 < i1; g0 += C::SB, ++ctr) {     // one ring stage: up to SB blocks
+        const int nb = min(C::SB, i1 - g0);
         const uint32_t st = ctr % NS, round = ctr / NS;
         if (!mbar_wait(full0 + 8 * st, round & 1)) set_error(d, kErrTimeout);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        const uint8_t* stage = ring + st * C::STAGE;
-        if constexpr (FP8) {
-          const uint8_t* kb = stage + kvh * kBlock * kD;
-          const uint4 r0a = lds128(kb + g * kD + (((2 * t) ^ g) << 4));
-          const uint4 r0b = lds128(kb + g * kD + (((2 * t + 1) ^ g) << 4));
-          const uint4 r1a = lds128(kb + (g + 8) * kD + (((2 * t) ^ g) << 4));
-          const uint4 r1b = lds128(kb + (g + 8) * kD + (((2 * t + 1) ^ g) << 4));
-          const uint32_t w0[8] = {r0a.x, r0a.y, r0a.z, r0a.w, r0b.x, r0b.y, r0b.z, r0b.w};
-          const uint32_t w1[8] = {r1a.x, r1a.y, r1a.z, r1a.w, r1b.x, r1b.y, r1b.z, r1b.w};
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            mma_f16(acc, e4m3x2_to_f16x2(w0[ks] & 0xffffu), e4m3x2_to_f16x2(w1[ks] & 0xffffu),
-                    e4m3x2_to_f16x2(w0[ks] >> 16), e4m3x2_to_f16x2(w1[ks] >> 16), qf[ks][0], qf[ks][1]);
-          }
-        } else {
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const int half = ks >> 2, c0 = (2 * ks) & 7;
-            const int m = lane >> 3, row = ((m & 1) << 3) + (lane & 7), chunk = c0 + (m >> 1);
-            const uint8_t* base = stage + half * C::HALF + kvh * kBlock * 128;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(smem_u32(base + row * 128 + ((chunk ^ (row & 7)) << 4)), a0, a1, a2, a3);
-            mma_bf16(acc, a0, a1, a2, a3, qf[ks][0], qf[ks][1]);
-          }
-        }
-        const int64_t p0 = (int64_t)blk_id[i] * kBlock;
-        float sc0 = P.qk_scale, sc1 = P.qk_scale;
-        if constexpr (FP8) {
-          const float* sk = sscale + st * kBlock;
-          sc0 *= sk[g];
-          sc1 *= sk[g + 8];
-        }
-        const bool v0 = p0 + g >= sb.lo && p0 + g < sb.next;
-        const bool v1 = p0 + g + 8 >= sb.lo && p0 + g + 8 < sb.next;
-        const float s00 = v0 ? acc[0] * sc0 : -INFINITY, s01 = v0 ? acc[1] * sc0 : -INFINITY;
-        const float s10 = v1 ? acc[2] * sc1 : -INFINITY, s11 = v1 ? acc[3] * sc1 : -INFINITY;
-        const int h0 = kvh * kG + 2 * t;
-        lgbase[lidx<HQ>(i, h0, g)] = s00;
-        lgbase[lidx<HQ>(i, h0 + 1, g)] = s01;
-        lgbase[lidx<HQ>(i, h0, g + 8)] = s10;
-        lgbase[lidx<HQ>(i, h0 + 1, g + 8)] = s11;
-        mx0 = fmaxf(mx0, fmaxf(s00, s10));
-        mx1 = fmaxf(mx1, fmaxf(s01, s11));
+        const uint8_t* stage = ring + (size_t)st * C::STAGE;
+        const float* sst = sscale + st * C::SB * kBlock;
+        int j = sub;
+        for (; j + WPK < nb; j += 2 * WPK)
+          qk_blocks<HKV, FP8, 2>(stage, sst, j, g0 + j, blk_id, qf, lgbase, kvh, lane, sb.lo, sb.next, P.qk_scale, mx0, mx1);
+        if (j < nb)
+          qk_blocks<HKV, FP8, 1>(stage, sst, j, g0 + j, blk_id, qf, lgbase, kvh, lane, sb.lo, sb.next, P.qk_scale, mx0, mx1);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
       }
@@ -392,55 +564,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       float o[8][4];
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
-      for (int i = i0; i < i1; ++i, ++ctr) {
-        if ((i & (WPK - 1)) != sub) continue;
+      for (int g0 = i0; g0 < i1; g0 += C::SB, ++ctr) {
+        const int nb = min(C::SB, i1 - g0);
         const uint32_t st = ctr % NS, round = ctr / NS;
         if (!mbar_wait(full0 + 8 * st, round & 1)) set_error(d, kErrTimeout);
-        const uint8_t* stage = ring + st * C::STAGE;
-        float2* pa = reinterpret_cast<float2*>(lgbase + lidx<HQ>(i, hg, 2 * t));
-        float2* pb = reinterpret_cast<float2*>(lgbase + lidx<HQ>(i, hg, 2 * t + 8));
-        const float2 sa = *pa, sbv = *pb;
-        const float p0 = exp2f(sa.x - mh), p1 = exp2f(sa.y - mh);
-        const float p8 = exp2f(sbv.x - mh), p9 = exp2f(sbv.y - mh);
-        lsum += (p0 + p1) + (p8 + p9);
-        *pa = make_float2(p0, p1);
-        *pb = make_float2(p8, p9);
-        if constexpr (FP8) {
-          const float* sv = sscale + st * kBlock;
-          const uint32_t b0 = pack_f16(p0 * sv[2 * t] * kVFold, p1 * sv[2 * t + 1] * kVFold);
-          const uint32_t b1 = pack_f16(p8 * sv[2 * t + 8] * kVFold, p9 * sv[2 * t + 9] * kVFold);
-          const uint8_t* vb = stage + kvh * kBlock * kD;
-          const uint4 L0 = lds128(vb + (2 * t) * kD + ((g ^ (2 * t)) << 4));
-          const uint4 L1 = lds128(vb + (2 * t + 1) * kD + ((g ^ (2 * t + 1)) << 4));
-          const uint4 L2 = lds128(vb + (2 * t + 8) * kD + ((g ^ (2 * t)) << 4));
-          const uint4 L3 = lds128(vb + (2 * t + 9) * kD + ((g ^ (2 * t + 1)) << 4));
-          const uint32_t x0[4] = {L0.x, L0.y, L0.z, L0.w}, y0[4] = {L1.x, L1.y, L1.z, L1.w};
-          const uint32_t x2[4] = {L2.x, L2.y, L2.z, L2.w}, y2[4] = {L3.x, L3.y, L3.z, L3.w};
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            const uint32_t lo = prmt(x0[w], y0[w], 0x5140), hi = prmt(x0[w], y0[w], 0x7362);
-            const uint32_t lo2 = prmt(x2[w], y2[w], 0x5140), hi2 = prmt(x2[w], y2[w], 0x7362);
-            mma_f16(o[2 * w], e4m3x2_to_f16x2(lo & 0xffffu), e4m3x2_to_f16x2(lo >> 16),
-                    e4m3x2_to_f16x2(lo2 & 0xffffu), e4m3x2_to_f16x2(lo2 >> 16), b0, b1);
-            mma_f16(o[2 * w + 1], e4m3x2_to_f16x2(hi & 0xffffu), e4m3x2_to_f16x2(hi >> 16),
-                    e4m3x2_to_f16x2(hi2 & 0xffffu), e4m3x2_to_f16x2(hi2 >> 16), b0, b1);
-          }
-        } else {
-          const float h0 = __bfloat162float(__float2bfloat16_rn(p0)), h1 = __bfloat162float(__float2bfloat16_rn(p1));
-          const float h8 = __bfloat162float(__float2bfloat16_rn(p8)), h9 = __bfloat162float(__float2bfloat16_rn(p9));
-          const uint32_t bh0 = pack_bf16(h0, h1), bh1 = pack_bf16(h8, h9);
-          const uint32_t bl0 = pack_bf16(p0 - h0, p1 - h1), bl1 = pack_bf16(p8 - h8, p9 - h9);
-#pragma unroll
-          for (int mb = 0; mb < 8; ++mb) {
-            const int half = mb >> 2, c0 = (2 * mb) & 7;
-            const int m = lane >> 3, pos = ((m >> 1) << 3) + (lane & 7), chunk = c0 + (m & 1);
-            const uint8_t* base = stage + half * C::HALF + kvh * kBlock * 128;
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4_t(smem_u32(base + pos * 128 + ((chunk ^ (pos & 7)) << 4)), a0, a1, a2, a3);
-            mma_bf16(o[mb], a0, a1, a2, a3, bh0, bh1);
-            mma_bf16(o[mb], a0, a1, a2, a3, bl0, bl1);
-          }
-        }
+        const uint8_t* stage = ring + (size_t)st * C::STAGE;
+        const float* sst = sscale + st * C::SB * kBlock;
+        int j = sub;
+        for (; j + WPK < nb; j += 2 * WPK)
+          pv_blocks<HKV, FP8, 2>(stage, sst, j, g0 + j, lgbase, bsum, kvh, lane, mh, lsum, o);
+        if (j < nb)
+          pv_blocks<HKV, FP8, 1>(stage, sst, j, g0 + j, lgbase, bsum, kvh, lane, mh, lsum, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
       }
@@ -452,7 +586,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) obuf[(kvh * 32 + mb * 4 + r) * 32 + lane] = o[mb][r];
+          for (int rr = 0; rr < 4; ++rr) obuf[(kvh * 32 + mb * 4 + rr) * 32 + lane] = o[mb][rr];
       }
       named_sync(1, kNCW * 32);
       if (sub == 0) {
@@ -460,7 +594,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 #pragma unroll
           for (int mb = 0; mb < 8; ++mb)
 #pragma unroll
-            for (int r = 0; r < 4; ++r) o[mb][r] += obuf[(kvh * 32 + mb * 4 + r) * 32 + lane];
+            for (int rr = 0; rr < 4; ++rr) o[mb][rr] += obuf[(kvh * 32 + mb * 4 + rr) * 32 + lane];
         }
         const float ofold = FP8 ? 1.0f / kVFold : 1.0f;
         float* rec = partials + (size_t)(c + b) * HQ * REC;
@@ -483,9 +617,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
           rec[(size_t)h * REC + 1] = l;
         }
       }
-      __threadfence();                 // every writer: partials visible GPU-wide ...
       named_sync(1, kNCW * 32);
-      if (tid == 0) atomicAdd(&arrive[s], 1);   // ... before the arrival
+      // release: the CTA barrier orders every writer's records before this fence
+      if (tid == 0) {
+        __threadfence();
+        atomicAdd(&arrive[s], 1);
+      }
       i0 = i1;
     }
 
@@ -506,55 +643,85 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       }
       named_sync(1, kNCW * 32);
       if (!flag[0]) break;
-      if (tid < HQ) {
-        float M = -INFINITY;
-        for (int pc = cf; pc <= cl; ++pc) M = fmaxf(M, __ldcg(partials + ((size_t)(pc + b) * HQ + tid) * REC));
-        float L = 0.f;
-        for (int pc = cf; pc <= cl; ++pc) {
-          const float* r = partials + ((size_t)(pc + b) * HQ + tid) * REC;
-          L += __ldcg(r + 1) * exp2f(__ldcg(r) - M);
+
+      // global normaliser of every head: rounds of kSC partial records loaded at once;
+      // with S <= kSC the records stay in pm / pl and become the output factors
+      float runM = -INFINITY, runL = 0.f, mown = -INFINITY;
+      for (int c0 = cf; c0 <= cl; c0 += kSC) {
+        const int nc = min(kSC, cl - c0 + 1);
+        for (int idx = tid; idx < nc * HQ; idx += kNCW * 32) {
+          const float* rp = partials + ((size_t)(c0 + idx / HQ + b) * HQ + idx % HQ) * REC;
+          pm[idx] = __ldcg(rp);
+          pl[idx] = __ldcg(rp + 1);
         }
-        const float mown = __ldcg(partials + ((size_t)(c + b) * HQ + tid) * REC);
-        cfac[tid] = exp2f(mown - M) / L;
-        gmax[tid] = M;
-        ginv[tid] = 1.0f / L;
+        named_sync(1, kNCW * 32);
+        if (tid < HQ) {
+          float cm = runM;
+          for (int k = 0; k < nc; ++k) cm = fmaxf(cm, pm[k * HQ + tid]);
+          float l = runL * exp2f(runM - cm);
+          for (int k = 0; k < nc; ++k) l += pl[k * HQ + tid] * exp2f(pm[k * HQ + tid] - cm);
+          runM = cm;
+          runL = l;
+          if (c >= c0 && c < c0 + nc) mown = pm[(c - c0) * HQ + tid];
+        }
+        if (c0 + kSC <= cl) named_sync(1, kNCW * 32);       // pm / pl are reloaded
+      }
+      if (tid < HQ) {
+        cfac[tid] = exp2f(mown - runM) / runL;
+        gmax[tid] = runM;
+        ginv[tid] = 1.0f / runL;
       }
       named_sync(1, kNCW * 32);
-      // masses: one warp per block; lanes 0-15 positions x heads [0, HQ/2), 16-31 the rest
-      for (int i = i0 + warp; i < i1; i += kNCW) {
-        const int j = lane & 15, hh = (lane >> 4) * (HQ / 2);
-        float tau = 0.f, bmax = 0.f;
-        for (int h = hh; h < hh + HQ / 2; ++h) {
-          const float a = lgbase[lidx<HQ>(i, h, j)] * cfac[h];
-          tau += a;
-          float bs = a;
-          bs += __shfl_xor_sync(0xffffffffu, bs, 1);
-          bs += __shfl_xor_sync(0xffffffffu, bs, 2);
-          bs += __shfl_xor_sync(0xffffffffu, bs, 4);
-          bs += __shfl_xor_sync(0xffffffffu, bs, 8);
-          bmax = fmaxf(bmax, bs);
+      const bool fac_in_smem = S <= kSC;
+      if (fac_in_smem)
+        for (int idx = tid; idx < S * HQ; idx += kNCW * 32) pm[idx] = exp2f(pm[idx] - gmax[idx % HQ]) * ginv[idx % HQ];
+      named_sync(1, kNCW * 32);
+
+      if (warp < kNCW / 2) {
+        // masses: one warp per block
+        for (int i = i0 + warp; i < i1; i += kNCW / 2) {
+          float bm = 0.f;                                   // block: max over heads
+          for (int h = lane; h < HQ; h += 32) bm = fmaxf(bm, bsum[i * HQ + h] * cfac[h]);
+#pragma unroll
+          for (int o2 = 16; o2 > 0; o2 >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
+          const int j = lane & 15, hh = (lane >> 4) * (HQ / 2);
+          float tau = 0.f;                                  // entry: sum over heads
+#pragma unroll 8
+          for (int h = hh; h < hh + HQ / 2; ++h) tau += lgbase[lidx<HQ>(i, h, j)] * cfac[h];
+          tau += __shfl_xor_sync(0xffffffffu, tau, 16);
+          const int64_t p = (int64_t)blk_id[i] * kBlock + j;
+          if (lane < 16 && p >= sb.lo && p < sb.next)       // slot of position p = p % 16
+            d.tok_mass[lay_slot + (size_t)blk_page[i] * kBlock + j] = tau;
+          if (lane == 0)
+            d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
         }
-        tau += __shfl_xor_sync(0xffffffffu, tau, 16);
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
-        const int64_t p = (int64_t)blk_id[i] * kBlock + j;
-        if (lane < 16 && p >= sb.lo && p < sb.next) {
-          int32_t slot;
-          const int32_t page = page_of(d, s, p, &slot);
-          d.tok_mass[lay_slot + (size_t)page * kBlock + slot] = tau;
-        }
-        if (lane == 0)
-          d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bmax;
-      }
-      // output: this CTA combines heads h with h % S == its rank among the sequence's CTAs
-      for (int h = c - cf; h < HQ; h += S) {
-        const float M = gmax[h], inv = ginv[h];
-        for (int dd = tid; dd < kD; dd += kNCW * 32) {
+      } else {
+        // output: this CTA combines heads h with h % S == its rank among the sequence's CTAs
+        const int rank = c - cf;
+        const int nh = rank < HQ ? (HQ - rank + S - 1) / S : 0;
+        const int ot = tid - (kNCW / 2) * 32;
+        for (int idx = ot; idx < nh * kD; idx += (kNCW / 2) * 32) {
+          const int h = rank + (idx / kD) * S, dd = idx % kD;
+          const float* r0 = partials + ((size_t)(cf + b) * HQ + h) * REC + 2 + dd;
           float acc = 0.f;
-          for (int pc = cf; pc <= cl; ++pc) {
-            const float* r = partials + ((size_t)(pc + b) * HQ + h) * REC;
-            acc += __ldcg(r + 2 + dd) * exp2f(__ldcg(r) - M);
+          if (fac_in_smem) {
+            for (int k0 = 0; k0 < S; k0 += 16) {                      // 16 loads in flight
+              float ov[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) ov[u] = (k0 + u < S) ? __ldcg(r0 + (size_t)(k0 + u) * HQ * REC) : 0.f;
+#pragma unroll
+              for (int u = 0; u < 16; ++u)
+                if (k0 + u < S) acc += ov[u] * pm[(k0 + u) * HQ + h];
+            }
+          } else {
+            const float M = gmax[h];
+            for (int k = 0; k < S; ++k) {
+              const float* rp = partials + ((size_t)(cf + k + b) * HQ + h) * REC;
+              acc += __ldcg(rp + 2 + dd) * exp2f(__ldcg(rp) - M);
+            }
+            acc *= ginv[h];
           }
-          P.out[((size_t)b * HQ + h) * kD + dd] = acc * inv;
+          P.out[((size_t)b * HQ + h) * kD + dd] = acc;
         }
       }
       named_sync(1, kNCW * 32);
@@ -574,29 +741,30 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 
 size_t tc_smem_limit() { return 227 * 1024; }
 
-template <int HKV, bool FP8, bool LSMEM>
-size_t smem_bytes(int cap, int n_seqs) {
-  using C = Cfg<HKV, FP8>;
-  size_t b = 1024;                                    // alignment slack
-  b += (size_t)C::NS * C::STAGE + C::NS * kBlock * 4 + 2 * C::NS * 8;
-  b += (size_t)3 * cap * 4 + (size_t)(n_seqs + 1) * 4;
-  b += (size_t)(2 * C::WPK + 4) * C::HQ * 4 + 16;
-  b += (C::WPK == 2 ? (size_t)HKV * 32 * 32 * 4 : 0) + 16;
-  if (LSMEM) b += (size_t)cap * C::HQ * kBlock * 4;
-  return b;
+// Ring stages that fit next to the rest of the carve-up (0 if fewer than kMinStages).
+int ring_stages(int hkv, bool fp8, bool lsmem, int cap, int n_seqs) {
+  const size_t blk = (size_t)hkv * kBlock * kD * (fp8 ? 1 : 2);
+  const size_t sb = kStageBytes / blk;
+  const size_t stage = sb * blk;
+  const size_t rest = plan_smem(hkv, fp8, lsmem, cap, n_seqs, 0).total;
+  if (rest >= tc_smem_limit()) return 0;
+  size_t ns = (tc_smem_limit() - rest) / (stage + sb * kBlock * 4 + 16);
+  ns = ns < (size_t)(kRingBytes / stage) ? ns : (size_t)(kRingBytes / stage);
+  return ns >= (size_t)kMinStages ? (int)ns : 0;
 }
 
 template <int HKV, bool FP8, bool LSMEM>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, const Params& P, int grid,
                        cudaStream_t st) {
   auto fn = attend_tc_kernel<HKV, FP8, LSMEM>;
-  const size_t smem = smem_bytes<HKV, FP8, LSMEM>(P.cap, P.n_seqs);
+  const size_t smem = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, P.ns).total;
   static bool attr_set = false;      // one opt-in per instantiation, to the full limit
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_limit());
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (smem > tc_smem_limit()) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -612,10 +780,11 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
 
 template <int HKV, bool FP8>
 cudaError_t launch_pick(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, Params P, int grid,
-                        size_t smem_limit, cudaStream_t st) {
-  if (smem_bytes<HKV, FP8, true>(P.cap, P.n_seqs) <= smem_limit)
-    return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
-  if (smem_bytes<HKV, FP8, false>(P.cap, P.n_seqs) > smem_limit) return cudaErrorInvalidConfiguration;
+                        cudaStream_t st) {
+  P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
+  if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
+  P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs);
+  if (P.ns == 0) return cudaErrorInvalidConfiguration;
   if ((size_t)grid * P.cap * Cfg<HKV, FP8>::HQ * kBlock > d.logit_scratch_elems) return cudaErrorInvalidConfiguration;
   return launch_one<HKV, FP8, false>(tk, tv, d, P, grid, st);
 }
@@ -633,10 +802,10 @@ bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
-    cudaDriverEntryPointQueryResult q;
+    cudaDriverEntryPointQueryResult qr;
     void* fn = nullptr;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
-    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
+    if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   const bool fp8 = kv_dtype == KVS_E4M3;
@@ -645,11 +814,11 @@ cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int
   cuuint64_t strides[3] = {(cuuint64_t)kD * esz, (cuuint64_t)kBlock * kD * esz, (cuuint64_t)Hkv * kBlock * kD * esz};
   cuuint32_t box[4] = {(cuuint32_t)(fp8 ? 128 : 64), (cuuint32_t)kBlock, (cuuint32_t)Hkv, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
-                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+  CUresult res = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                        const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return res == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 // Blocks one CTA must hold for a launch whose resident blocks number at most T_bound.
@@ -664,14 +833,13 @@ cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   P.n_seqs = n_seqs;
   P.cap = tc_cap(T_bound, grid);
   if (P.cap < 1) P.cap = 1;
+  P.ns = 0;
   P.q = q;
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
-  const size_t lim = tc_smem_limit();
   const bool fp8 = d.kv_dtype == KVS_E4M3;
-  if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, P, grid, lim, st)
-                             : launch_pick<4, false>(tk, tv, d, P, grid, lim, st);
-  return fp8 ? launch_pick<8, true>(tk, tv, d, P, grid, lim, st) : launch_pick<8, false>(tk, tv, d, P, grid, lim, st);
+  if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, P, grid, st) : launch_pick<4, false>(tk, tv, d, P, grid, st);
+  return fp8 ? launch_pick<8, true>(tk, tv, d, P, grid, st) : launch_pick<8, false>(tk, tv, d, P, grid, st);
 }
 
 // Largest grid the cooperative launch allows with one CTA per SM.
@@ -757,9 +925,8 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
   const bool fp8 = d.kv_dtype == KVS_E4M3;
-  const size_t need_smem = d.Hkv == 4 ? (fp8 ? smem_bytes<4, true, true>(P.cap, n_seqs) : smem_bytes<4, false, true>(P.cap, n_seqs))
-                                      : (fp8 ? smem_bytes<8, true, true>(P.cap, n_seqs) : smem_bytes<8, false, true>(P.cap, n_seqs));
-  if (need_smem > tc_smem_limit()) return cudaErrorNotSupported;
+  P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+  if (P.ns == 0) return cudaErrorNotSupported;
   void* base = nullptr;
   cudaError_t e = static_scratch_address(&base);
   if (e != cudaSuccess) return e;

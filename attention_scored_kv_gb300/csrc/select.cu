@@ -9,9 +9,10 @@
 //
 // One CTA per sequence.  Candidates are enumerated in ascending block id.  Each gets a
 // 64-bit key that orders like its float64 score (protected blocks get the largest
-// key); an MSB-first radix select over the key bytes finds the key T of the k-th best
-// and how many of the candidates equal to T to take; a stable compaction in id order
-// then emits every key > T and the first ties in id order, ascending.
+// key); the keys are kept in shared memory when they fit.  An MSB-first radix select
+// over the key bytes (histogram in shared memory, bucket found by one warp scan) finds
+// the key T of the k-th best and how many candidates equal to T to take; a stable
+// compaction in id order then emits every key > T and the first ties in id order.
 #include "kvs_internal.cuh"
 
 namespace kvs {
@@ -19,6 +20,7 @@ namespace kvs {
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kSmemCap = 6144;          // candidates whose keys stay in shared memory
 
 __device__ __forceinline__ uint64_t order_key(double v) {
   const uint64_t b = (uint64_t)__double_as_longlong(v);
@@ -31,7 +33,6 @@ struct SelShared {
   uint64_t prefix;
   int32_t remaining;
   int32_t n_prot;
-  int32_t base;
 };
 
 __device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlocks& sb, int i, int kind,
@@ -50,7 +51,8 @@ __device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlock
     v = d.c_blk[t];
   } else {
     const int32_t last = d.last_blk[t];
-    v = (last < 0) ? 0.0 : d.e_blk[t] * pow(d.ema_decay, (double)(d.steps[s] - 1 - last));
+    const int32_t gap = d.steps[s] - 1 - last;
+    v = (last < 0) ? 0.0 : (gap == 0 ? d.e_blk[t] : d.e_blk[t] * pow(d.ema_decay, (double)gap));
   }
   return order_key(v);
 }
@@ -78,51 +80,81 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
                                                             int k_uniform, int kind, uint32_t flags, int32_t* keep_ids,
                                                             int keep_capacity, int32_t* keep_count) {
   __shared__ SelShared sh;
+  extern __shared__ uint8_t dyn[];
+  uint64_t* skey = reinterpret_cast<uint64_t*>(dyn);                 // [kSmemCap]
+  int32_t* sid = reinterpret_cast<int32_t*>(skey + kSmemCap);        // [kSmemCap]
+  int32_t* spage = sid + kSmemCap;                                   // [kSmemCap]
   const int sl = blockIdx.x, s = seq_begin + sl;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int n = sb.n;
   const bool protect = (flags & KVS_SELECT_PROTECT) != 0;
   const bool apply = (flags & KVS_SELECT_APPLY) != 0 && d.mode == KVS_MODE_H2O;
+  const bool in_smem = n <= kSmemCap;
   int kk = k_per_seq ? k_per_seq[sl] : k_uniform;
   if (kk < 0) kk = 0;
 
-  // protected count
-  if (threadIdx.x == 0) sh.n_prot = 0;
+  // keys (into shared memory when they fit) and the protected count
+  if (tid == 0) sh.n_prot = 0;
   __syncthreads();
-  if (protect) {
-    int cnt = 0;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      int32_t k, page;
-      cnt += cand_key(d, s, sb, i, kind, true, &k, &page) == ~0ull;
-    }
-    atomicAdd(&sh.n_prot, cnt);
-    __syncthreads();
-    if (kk < sh.n_prot) kk = sh.n_prot;
+  int cnt = 0;
+  for (int i = tid; i < n; i += kThreads) {
+    int32_t k, page;
+    const uint64_t key = cand_key(d, s, sb, i, kind, protect, &k, &page);
+    cnt += key == ~0ull;
+    if (in_smem) { skey[i] = key; sid[i] = k; spage[i] = page; }
   }
+  if (protect) atomicAdd(&sh.n_prot, cnt);
+  __syncthreads();
+  if (kk < sh.n_prot) kk = sh.n_prot;
   const bool keep_all = kk >= n;
 
-  // radix select of the kk-th largest key
-  if (threadIdx.x == 0) { sh.prefix = 0; sh.remaining = kk; }
+  auto key_of = [&](int i, int32_t* k, int32_t* page) -> uint64_t {
+    if (in_smem) { *k = sid[i]; *page = spage[i]; return skey[i]; }
+    return cand_key(d, s, sb, i, kind, protect, k, page);
+  };
+
+  // radix select of the kk-th largest key (k = 0 keeps nothing: T above every key)
+  if (tid == 0) { sh.prefix = kk > 0 ? 0ull : ~0ull; sh.remaining = 0; }
+  if (tid == 0 && kk > 0) sh.remaining = kk;
   uint64_t mask = 0;
-  if (!keep_all) {
+  if (!keep_all && kk > 0) {
     for (int shift = 56; shift >= 0; shift -= 8) {
-      for (int b = threadIdx.x; b < 256; b += kThreads) sh.hist[b] = 0;
+      for (int b = tid; b < 256; b += kThreads) sh.hist[b] = 0;
       __syncthreads();
       const uint64_t prefix = sh.prefix;
-      for (int i = threadIdx.x; i < n; i += kThreads) {
+      for (int i = tid; i < n; i += kThreads) {
         int32_t k, page;
-        const uint64_t key = cand_key(d, s, sb, i, kind, protect, &k, &page);
+        const uint64_t key = key_of(i, &k, &page);
         if ((key & mask) == prefix) atomicAdd(&sh.hist[(key >> shift) & 255u], 1u);
       }
       __syncthreads();
-      if (threadIdx.x == 0) {
-        int rem = sh.remaining;
-        for (int b = 255; b >= 0; --b) {
-          const int c = (int)sh.hist[b];
-          if (c >= rem) { sh.prefix = prefix | ((uint64_t)b << shift); break; }
-          rem -= c;
+      if (warp == 0) {
+        // lane l owns buckets 255-8l .. 248-8l (descending); find the bucket holding the
+        // remaining-th largest key with one scan over the lanes
+        const int rem = sh.remaining;
+        int c8[8], local = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) { c8[u] = (int)sh.hist[255 - 8 * lane - u]; local += c8[u]; }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
         }
-        sh.remaining = rem;
+        const int excl = incl - local;
+        const unsigned m = __ballot_sync(0xffffffffu, excl < rem && incl >= rem);
+        const int src = m ? __ffs(m) - 1 : 31;
+        if (lane == src) {
+          int r2 = rem - excl, bucket = 248 - 8 * lane;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (c8[u] >= r2) { bucket = 255 - 8 * lane - u; break; }
+            r2 -= c8[u];
+          }
+          sh.prefix = prefix | ((uint64_t)bucket << shift);
+          sh.remaining = r2;
+        }
       }
       mask |= 255ull << shift;
       __syncthreads();
@@ -133,13 +165,12 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
 
   // stable compaction in id order (chunks of kThreads); eviction rewrites the list
   int kept_before = 0, eq_before = 0;
-  if (threadIdx.x == 0) sh.base = 0;
   for (int c0 = 0; c0 < n; c0 += kThreads) {
-    const int i = c0 + threadIdx.x;
+    const int i = c0 + tid;
     int32_t k = -1, page = -1;
     uint64_t key = 0;
     const bool live = i < n;
-    if (live) key = cand_key(d, s, sb, i, kind, protect, &k, &page);
+    if (live) key = key_of(i, &k, &page);
     int eq_total;
     const int is_eq = (!keep_all && live && key == T) ? 1 : 0;
     const int eq_rank = eq_before + block_scan(is_eq, sh, &eq_total);
@@ -164,7 +195,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
     }
     __syncthreads();
   }
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     keep_count[sl] = kept_before;
     if (apply) d.res_count[s] = kept_before;
   }
@@ -175,8 +206,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
 cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
                           int32_t* keep_count, cudaStream_t st) {
-  select_kernel<<<n_seqs, kThreads, 0, st>>>(d, seq_begin, k_per_seq, k_uniform, score_kind, flags, keep_ids,
-                                             keep_capacity, keep_count);
+  const size_t smem = (size_t)kSmemCap * (8 + 4 + 4);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  select_kernel<<<n_seqs, kThreads, smem, st>>>(d, seq_begin, k_per_seq, k_uniform, score_kind, flags, keep_ids,
+                                                keep_capacity, keep_count);
   return cudaGetLastError();
 }
 
