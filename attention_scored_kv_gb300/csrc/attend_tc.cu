@@ -46,6 +46,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kG = 8;
 constexpr int kNCW = 8;                 // consumer warps
+constexpr int kRec = kD + 4;            // partial record of one head: m, l, 2 pad, o[kD] (16-byte rows)
 constexpr int kThreads = (kNCW + 1) * 32;
 constexpr int kMbarLimit = 1 << 22;     // polls of an mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
@@ -349,8 +350,8 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   p.ring = o;   o += (size_t)ns * sb * blk;
   p.sscale = o; o += (size_t)ns * sb * kBlock * 4;
   p.bars = o;   o += (size_t)2 * ns * 8;
-  p.blk = o;    o = up16(o + (size_t)3 * cap * 4);
-  p.prefix = o; o = up16(o + (size_t)(n_seqs + 1) * 4);
+  p.blk = o;    o = up16(o + (size_t)4 * cap * 4);
+  p.prefix = o; o = up16(o + (size_t)2 * (n_seqs + 1) * 4);    // prefix, then cst
   p.mbuf = o;   o += (size_t)WPK * HQ * 4;
   p.lbuf = o;   o += (size_t)WPK * HQ * 4;
   p.hv = o;     o += (size_t)4 * HQ * 4;
@@ -369,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Dev d, const Params P) {
   using C = Cfg<HKV, FP8>;
-  constexpr int HQ = C::HQ, WPK = C::WPK, REC = kD + 2;
+  constexpr int HQ = C::HQ, WPK = C::WPK, REC = kRec;
   const int NS = P.ns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -380,7 +381,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   int32_t* blk_id = reinterpret_cast<int32_t*>(smem + sp.blk);
   int32_t* blk_page = blk_id + P.cap;
   int32_t* blk_seq = blk_page + P.cap;
+  int32_t* ticket = blk_seq + P.cap;                                   // arrival order, by segment start
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + sp.prefix);       // [n_seqs + 1]
+  int32_t* cst = prefix + P.n_seqs + 1;                                 // [n_seqs + 1]
   float* mbuf = reinterpret_cast<float*>(smem + sp.mbuf);              // [WPK][HQ]
   float* lbuf = reinterpret_cast<float*>(smem + sp.lbuf);              // [WPK][HQ]
   float* mseg = reinterpret_cast<float*>(smem + sp.hv);                // [HQ]
@@ -415,14 +418,70 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       run += __shfl_sync(0xffffffffu, incl, 31);
     }
     if (lane == 0) prefix[P.n_seqs] = run;
+    __syncwarp();
+    // Whole CTAs per sequence: X = the fewest blocks per CTA such that ceil(n_b / X)
+    // CTAs for every sequence b take at most G CTAs.  Each CTA then holds one segment
+    // (one flush, one combine), so no CTA does two sequences' work in series.  Taken
+    // when X is within the per-CTA capacity; otherwise the blocks are split end to end.
+    int X = 0;
+    if (P.n_seqs <= G && run > 0) {
+      auto ctas_for = [&](int x) {
+        int cnt = 0;
+        for (int b = lane; b < P.n_seqs; b += 32) cnt += (prefix[b + 1] - prefix[b] + x - 1) / x;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
+        return cnt;
+      };
+      int lo = (run + G - 1) / G, hi = P.cap;
+      if (lo <= hi && ctas_for(hi) <= G) {
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (ctas_for(mid) <= G) hi = mid; else lo = mid + 1;
+        }
+        X = lo;
+        int crun = 0;
+        for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
+          const int b = b0 + lane;
+          const int cb = b < P.n_seqs ? (prefix[b + 1] - prefix[b] + X - 1) / X : 0;
+          int incl = cb;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+          }
+          if (b < P.n_seqs) cst[b] = crun + incl - cb;
+          crun += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) cst[P.n_seqs] = crun;
+      }
+    }
+    if (lane == 0) flag[1] = X;
   }
   __syncthreads();
-  // CTA c takes q + (c < r) consecutive blocks (T = q*G + r): no empty CTA ever sits
-  // between two non-empty ones, so a sequence's CTAs are a gap-free range.
+  const int X = flag[1];
   const int64_t T = prefix[P.n_seqs];
   const int64_t q = T / G, r = T % G;
-  const int64_t x0 = (int64_t)c * q + (c < r ? c : r);
-  const int nblk = (int)(q + (c < r ? 1 : 0));
+  int64_t x0 = 0;
+  int nblk = 0;
+  if (X > 0) {
+    // sequence b owns CTAs [cst[b], cst[b+1]); its blocks are split evenly over them
+    if (c < cst[P.n_seqs]) {
+      int lo = 0, hi = P.n_seqs - 1;        // last b with cst[b] <= c
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cst[mid] <= c) lo = mid; else hi = mid - 1;
+      }
+      const int S = cst[lo + 1] - cst[lo], rk = c - cst[lo];
+      const int nb = prefix[lo + 1] - prefix[lo], qb = nb / S, rb = nb % S;
+      x0 = prefix[lo] + (int64_t)rk * qb + (rk < rb ? rk : rb);
+      nblk = qb + (rk < rb ? 1 : 0);
+    }
+  } else {
+    // CTA c takes q + (c < r) consecutive blocks (T = q*G + r): no empty CTA ever sits
+    // between two non-empty ones, so a sequence's CTAs are a gap-free range.
+    x0 = (int64_t)c * q + (c < r ? c : r);
+    nblk = (int)(q + (c < r ? 1 : 0));
+  }
   if (nblk > P.cap) {                       // the host's bound was too small
     if (tid == 0) set_error(d, kErrCapacity);
     return;
@@ -599,15 +658,26 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const float ofold = FP8 ? 1.0f / kVFold : 1.0f;
         float* rec = partials + (size_t)(c + b) * HQ * REC;
         const int ha = kvh * kG + 2 * t;
+        if constexpr (FP8) {
+          // accumulator rows g, g+8 of tile mb hold dims 16g + 2mb and 16g + 2mb + 1:
+          // this thread owns dims 16g .. 16g+15 of heads ha and ha+1 (four 16-byte rows)
 #pragma unroll
-        for (int mb = 0; mb < 8; ++mb) {
-          int da, db;   // dims of accumulator rows g and g+8
-          if constexpr (FP8) { da = 16 * g + 2 * mb; db = da + 1; }
-          else { da = 16 * mb + g; db = da + 8; }
-          rec[(size_t)ha * REC + 2 + da] = o[mb][0] * ofold;
-          rec[(size_t)(ha + 1) * REC + 2 + da] = o[mb][1] * ofold;
-          rec[(size_t)ha * REC + 2 + db] = o[mb][2] * ofold;
-          rec[(size_t)(ha + 1) * REC + 2 + db] = o[mb][3] * ofold;
+          for (int j = 0; j < 4; ++j) {
+            float* ra = rec + (size_t)ha * REC + 4 + 16 * g + 4 * j;
+            *reinterpret_cast<float4*>(ra) = make_float4(o[2 * j][0] * ofold, o[2 * j][2] * ofold,
+                                                         o[2 * j + 1][0] * ofold, o[2 * j + 1][2] * ofold);
+            *reinterpret_cast<float4*>(ra + REC) = make_float4(o[2 * j][1] * ofold, o[2 * j][3] * ofold,
+                                                               o[2 * j + 1][1] * ofold, o[2 * j + 1][3] * ofold);
+          }
+        } else {
+#pragma unroll
+          for (int mb = 0; mb < 8; ++mb) {
+            const int da = 16 * mb + g, db = da + 8;   // dims of accumulator rows g and g+8
+            rec[(size_t)ha * REC + 4 + da] = o[mb][0];
+            rec[(size_t)(ha + 1) * REC + 4 + da] = o[mb][1];
+            rec[(size_t)ha * REC + 4 + db] = o[mb][2];
+            rec[(size_t)(ha + 1) * REC + 4 + db] = o[mb][3];
+          }
         }
         if (lane < kG) {
           const int h = kvh * kG + lane;
@@ -621,7 +691,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       // release: the CTA barrier orders every writer's records before this fence
       if (tid == 0) {
         __threadfence();
-        atomicAdd(&arrive[s], 1);
+        ticket[i0] = atomicAdd(&arrive[s], 1);
       }
       i0 = i1;
     }
@@ -633,10 +703,18 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
       const int b = blk_seq[i0], s = P.seq_begin + b;
       const SeqBlocks sb = seq_blocks(d, P.layer, s);
-      const int cf = cta_of(prefix[b], q, r), cl = cta_of(prefix[b + 1] - 1, q, r);
+      int cf, cl;                                  // the sequence's CTAs
+      if (X > 0) {
+        cf = cst[b];
+        cl = cst[b + 1] - 1;
+      } else {
+        cf = cta_of(prefix[b], q, r);
+        cl = cta_of(prefix[b + 1] - 1, q, r);
+      }
       const int S = cl - cf + 1;
       if (tid == 0) {
-        const bool ok = wait_at_least(&arrive[s], S, d.spin_limit);
+        // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
+        const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1 : wait_at_least(&arrive[s], S, d.spin_limit);
         __threadfence();
         flag[0] = ok ? 1 : 0;
         if (!ok) set_error(d, kErrTimeout);
@@ -702,7 +780,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const int ot = tid - (kNCW / 2) * 32;
         for (int idx = ot; idx < nh * kD; idx += (kNCW / 2) * 32) {
           const int h = rank + (idx / kD) * S, dd = idx % kD;
-          const float* r0 = partials + ((size_t)(cf + b) * HQ + h) * REC + 2 + dd;
+          const float* r0 = partials + ((size_t)(cf + b) * HQ + h) * REC + 4 + dd;
           float acc = 0.f;
           if (fac_in_smem) {
             for (int k0 = 0; k0 < S; k0 += 16) {                      // 16 loads in flight
@@ -717,7 +795,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             const float M = gmax[h];
             for (int k = 0; k < S; ++k) {
               const float* rp = partials + ((size_t)(cf + k + b) * HQ + h) * REC;
-              acc += __ldcg(rp + 2 + dd) * exp2f(__ldcg(rp) - M);
+              acc += __ldcg(rp + 4 + dd) * exp2f(__ldcg(rp) - M);
             }
             acc *= ginv[h];
           }
@@ -778,9 +856,18 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
   return cudaLaunchKernelEx(&cfg, fn, tk, tv, d, P);
 }
 
+// Per-CTA block capacity that leaves the partition room to give every sequence whole
+// CTAs (up to an eighth more blocks than an even split, plus two).
+int wide_cap(int base) { return base + base / 8 + 2; }
+
 template <int HKV, bool FP8>
 cudaError_t launch_pick(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, Params P, int grid,
                         cudaStream_t st) {
+  const int base = P.cap;
+  P.cap = wide_cap(base);                  // room for whole CTAs per sequence
+  P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
+  if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
+  P.cap = base;
   P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
   if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
   P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs);
@@ -884,7 +971,7 @@ size_t static_scratch_limit() { return kStaticScratchBytes; }
 // Bytes of the array one launch uses: records for CTA + sequence index < grid + n_seqs,
 // then 2 * max_seqs counters (indexed by absolute sequence).
 size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* counters_offset) {
-  const size_t rec = (size_t)(grid + n_seqs) * d.Hq * (kD + 2) * sizeof(float);
+  const size_t rec = (size_t)(grid + n_seqs) * d.Hq * kRec * sizeof(float);
   const size_t off = (rec + 255) & ~size_t(255);
   *counters_offset = off;
   return off + 2 * (size_t)d.max_seqs * sizeof(int32_t);
@@ -925,7 +1012,13 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
   const bool fp8 = d.kv_dtype == KVS_E4M3;
+  const int cap0 = P.cap;
+  P.cap = wide_cap(cap0);
   P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+  if (P.ns == 0) {
+    P.cap = cap0;
+    P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+  }
   if (P.ns == 0) return cudaErrorNotSupported;
   void* base = nullptr;
   cudaError_t e = static_scratch_address(&base);

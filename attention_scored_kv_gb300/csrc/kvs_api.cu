@@ -155,7 +155,7 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->last_blk = take(B * MB * 4);
   p->steps = take(B * 4);
   p->acc_tickets = take(B * 4);
-  p->partials = take(((size_t)kGridMax + B) * Hq * (D + 2) * 4);
+  p->partials = take(((size_t)kGridMax + B) * Hq * (D + 4) * 4);
   p->counters = take(2 * B * 4);
   p->logits = take(p->logit_elems * 4);
   p->err = take(4);
@@ -269,7 +269,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.max_seqs = cfg->max_seqs; d.max_positions = cfg->max_positions; d.max_blocks = p.max_blocks;
   d.window = cfg->window; d.mode = p.mode; d.num_pages = p.num_pages; d.pages_per_seq = p.pages_per_seq;
   d.kv_dtype = cfg->kv_dtype; d.in_dtype = cfg->in_dtype;
-  d.spin_limit = cfg->spin_limit == 0 ? kDefaultSpin : (cfg->spin_limit < 0 ? 0 : cfg->spin_limit);
+  d.spin_limit = cfg->spin_limit == 0 ? kDefaultSpin : cfg->spin_limit;
   d.h2o_sink_tokens = cfg->h2o_sink_tokens; d.h2o_recent_tokens = p.recent_tokens;
   d.ema_decay = cfg->ema_decay;
   const size_t slots = (size_t)p.num_pages * kBlock;

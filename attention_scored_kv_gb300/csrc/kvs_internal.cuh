@@ -14,7 +14,7 @@
 //     resident count [max_seqs]; free page stack [num_pages] + top
 //     score tables C/E per token [max_seqs][max_positions] double, stamp int32;
 //     C/E per block [max_seqs][max_blocks] double, stamp int32; steps [max_seqs] int32
-//     attend partials [(grid_max + max_seqs)][Hq][D + 2] float; arrival counters
+//     attend partials [(grid_max + max_seqs)][Hq][D + 4] float; arrival counters
 //     logit scratch (the general kernel, and the tensor kernel when logits do not fit
 //     in shared memory); accumulate tickets; the error word.
 #pragma once
@@ -43,7 +43,7 @@ struct Dev {
   int32_t max_seqs, max_positions, max_blocks;
   int32_t window, mode, num_pages, pages_per_seq;
   int32_t kv_dtype, in_dtype;
-  int32_t spin_limit;
+  int32_t spin_limit;     // polls of a device wait; -1: no wait (only the last arrival goes on)
   int32_t h2o_sink_tokens, h2o_recent_tokens;
   double ema_decay;
   // per-layer arrays: base pointer + per-layer stride in elements
@@ -65,7 +65,7 @@ struct Dev {
   double* c_blk; double* e_blk; int32_t* last_blk;   // [max_seqs][max_blocks]
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
-  float* partials;        // [(kGridMax + max_seqs)][Hq][D + 2]
+  float* partials;        // [(kGridMax + max_seqs)][Hq][D + 4]
   int32_t* counters;      // [2][max_seqs] arrivals, departures
   float* logit_scratch;   size_t logit_scratch_elems;
   int32_t* err;           // [1]
