@@ -27,11 +27,11 @@
 //   * Two passes per segment: all K blocks first (logits to shared memory, exact local
 //     max), then all V blocks (p = exp2(s - m), written back in place, and PV) - no
 //     rescaling of accumulators.
-//   * Each CTA publishes (m, l, o) per head and segment, arrives on a per-sequence
-//     counter, waits (bounded) until every CTA of the sequence has arrived, combines
-//     the global normaliser, converts its own on-chip p into the final weights and
-//     reduces them to the entry and block masses; the CTAs of a sequence share the
-//     output combine.  The last CTA to leave resets the counters for the next launch.
+//   * Each CTA publishes its partial output rows and (m, l) words per head and segment,
+//     arrives on a per-sequence counter, waits (bounded) until every CTA of the sequence
+//     has arrived, combines the global normaliser, converts its own on-chip p into the
+//     final weights and reduces them to the entry and block masses; the CTAs of a
+//     sequence share the output combine.  The last CTA to leave resets the counters.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -46,7 +46,6 @@ namespace {
 constexpr int kD = 128;
 constexpr int kG = 8;
 constexpr int kNCW = 8;                 // consumer warps
-constexpr int kRec = kD + 4;            // partial record of one head: m, l, 2 pad, o[kD] (16-byte rows)
 constexpr int kThreads = (kNCW + 1) * 32;
 constexpr int kMbarLimit = 1 << 22;     // polls of an mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
@@ -100,8 +99,16 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
+// Named barrier over n threads.  Every call site follows code that one thread or one
+// lane runs alone (a wait, an atomic), so the warp is first reconverged and the
+// non-aligned form is used: nothing here relies on the compiler having reconverged a
+// warp before an inline-asm barrier.
 __device__ __forceinline__ void named_sync(int id, int n) {
-  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+  __syncwarp();
+  asm volatile("barrier.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void red_add(int32_t* p, int32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
 
@@ -153,9 +160,9 @@ __device__ __forceinline__ int lidx(int i, int h, int pos) {
 }
 
 // CTA holding global block x when CTA c holds q + (c < r) blocks.
-__device__ __forceinline__ int cta_of(int64_t x, int64_t q, int64_t r) {
-  const int64_t big = r * (q + 1);
-  return (int)(x < big ? x / (q + 1) : r + (x - big) / q);
+__device__ __forceinline__ int cta_of(int x, int q, int r) {
+  const int big = r * (q + 1);
+  return x < big ? x / (q + 1) : r + (x - big) / q;
 }
 
 // QK^T of NB (1 or 2) blocks of one ring stage for one KV head, interleaved for ILP:
@@ -336,7 +343,7 @@ struct Params {
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
 // so every stage keeps the 1024-byte alignment the 128-byte swizzle needs.
 struct SmemPlan {
-  size_t ring, sscale, bars, blk, prefix, mbuf, lbuf, hv, flag, pm, pl, bsum, obuf, lg, total;
+  size_t ring, sscale, bars, seqb, blk, prefix, mbuf, lbuf, hv, flag, pm, pl, bsum, obuf, lg, total;
 };
 
 __host__ __device__ inline size_t up16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -350,6 +357,7 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   p.ring = o;   o += (size_t)ns * sb * blk;
   p.sscale = o; o += (size_t)ns * sb * kBlock * 4;
   p.bars = o;   o += (size_t)2 * ns * 8;
+  p.seqb = o;   o = up16(o + (size_t)n_seqs * sizeof(SeqBlocks));
   p.blk = o;    o = up16(o + (size_t)4 * cap * 4);
   p.prefix = o; o = up16(o + (size_t)2 * (n_seqs + 1) * 4);    // prefix, then cst
   p.mbuf = o;   o += (size_t)WPK * HQ * 4;
@@ -366,11 +374,13 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
 }
 
 template <int HKV, bool FP8, bool LSMEM>
-__global__ void __launch_bounds__(kThreads, 1)
+// 9 warps: one of the 4 schedulers holds 3 of them, and each scheduler has 16K registers,
+// so 168 per thread is the most one CTA per SM can have
+__global__ void __maxnreg__(168)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Dev d, const Params P) {
   using C = Cfg<HKV, FP8>;
-  constexpr int HQ = C::HQ, WPK = C::WPK, REC = kRec;
+  constexpr int HQ = C::HQ, WPK = C::WPK;
   const int NS = P.ns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -378,6 +388,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   uint8_t* ring = smem + sp.ring;
   float* sscale = reinterpret_cast<float*>(smem + sp.sscale);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.bars);          // full[NS], empty[NS]
+  SeqBlocks* seqb = reinterpret_cast<SeqBlocks*>(smem + sp.seqb);        // [n_seqs]
   int32_t* blk_id = reinterpret_cast<int32_t*>(smem + sp.blk);
   int32_t* blk_page = blk_id + P.cap;
   int32_t* blk_seq = blk_page + P.cap;
@@ -407,7 +418,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
       const int b = b0 + lane;
       int nb = 0;
-      if (b < P.n_seqs) nb = seq_blocks(d, P.layer, P.seq_begin + b).n;
+      if (b < P.n_seqs) {
+        const SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
+        seqb[b] = sb;
+        nb = sb.n;
+      }
       int incl = nb;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -419,36 +434,46 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     }
     if (lane == 0) prefix[P.n_seqs] = run;
     __syncwarp();
-    // Whole CTAs per sequence: X = the fewest blocks per CTA such that ceil(n_b / X)
-    // CTAs for every sequence b take at most G CTAs.  Each CTA then holds one segment
-    // (one flush, one combine), so no CTA does two sequences' work in series.  Taken
-    // when X is within the per-CTA capacity; otherwise the blocks are split end to end.
+    // Whole CTAs per sequence: with X blocks per CTA at most, sequence b takes
+    // ceil(n_b / X) CTAs; any X whose total is at most G will do.  Each CTA then holds
+    // one segment (one flush, one combine), so no CTA does two sequences' work in
+    // series.  X starts from an estimate that leaves half a CTA of slack per sequence;
+    // the split falls back to blocks end to end when no X within the per-CTA capacity
+    // fits.  ctas_for leaves each sequence's count in cst[].
     int X = 0;
     if (P.n_seqs <= G && run > 0) {
       auto ctas_for = [&](int x) {
         int cnt = 0;
-        for (int b = lane; b < P.n_seqs; b += 32) cnt += (prefix[b + 1] - prefix[b] + x - 1) / x;
+        for (int b = lane; b < P.n_seqs; b += 32) {
+          const int cb = (prefix[b + 1] - prefix[b] + x - 1) / x;
+          cst[b] = cb;
+          cnt += cb;
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
         return cnt;
       };
-      int lo = (run + G - 1) / G, hi = P.cap;
-      if (lo <= hi && ctas_for(hi) <= G) {
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (ctas_for(mid) <= G) hi = mid; else lo = mid + 1;
-        }
-        X = lo;
+      const int lo = (run + G - 1) / G, hi = P.cap;
+      int x = (2 * run + (2 * G - P.n_seqs) - 1) / (2 * G - P.n_seqs);   // ceil(T / (G - n/2))
+      if (x < lo) x = lo;
+      for (int it = 0; it < 3 && x < hi; ++it) {
+        if (ctas_for(x) <= G) { X = x; break; }
+        x += 1 + x / 16;
+      }
+      if (X == 0 && lo <= hi && ctas_for(hi) <= G) X = hi;
+      __syncwarp();
+      if (X > 0) {
         int crun = 0;
         for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
           const int b = b0 + lane;
-          const int cb = b < P.n_seqs ? (prefix[b + 1] - prefix[b] + X - 1) / X : 0;
+          const int cb = b < P.n_seqs ? cst[b] : 0;
           int incl = cb;
 #pragma unroll
           for (int o = 1; o < 32; o <<= 1) {
             const int v = __shfl_up_sync(0xffffffffu, incl, o);
             if (lane >= o) incl += v;
           }
+          __syncwarp();
           if (b < P.n_seqs) cst[b] = crun + incl - cb;
           crun += __shfl_sync(0xffffffffu, incl, 31);
         }
@@ -459,10 +484,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   }
   __syncthreads();
   const int X = flag[1];
-  const int64_t T = prefix[P.n_seqs];
-  const int64_t q = T / G, r = T % G;
-  int64_t x0 = 0;
-  int nblk = 0;
+  const int T = prefix[P.n_seqs];
+  const int q = T / G, r = T % G;
+  int x0 = 0;
+  int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole-CTA split)
   if (X > 0) {
     // sequence b owns CTAs [cst[b], cst[b+1]); its blocks are split evenly over them
     if (c < cst[P.n_seqs]) {
@@ -473,32 +498,35 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       }
       const int S = cst[lo + 1] - cst[lo], rk = c - cst[lo];
       const int nb = prefix[lo + 1] - prefix[lo], qb = nb / S, rb = nb % S;
-      x0 = prefix[lo] + (int64_t)rk * qb + (rk < rb ? rk : rb);
+      x0 = prefix[lo] + rk * qb + (rk < rb ? rk : rb);
       nblk = qb + (rk < rb ? 1 : 0);
+      cseq = lo;
     }
   } else {
     // CTA c takes q + (c < r) consecutive blocks (T = q*G + r): no empty CTA ever sits
     // between two non-empty ones, so a sequence's CTAs are a gap-free range.
-    x0 = (int64_t)c * q + (c < r ? c : r);
-    nblk = (int)(q + (c < r ? 1 : 0));
+    x0 = c * q + (c < r ? c : r);
+    nblk = q + (c < r ? 1 : 0);
   }
   if (nblk > P.cap) {                       // the host's bound was too small
     if (tid == 0) set_error(d, kErrCapacity);
     return;
   }
   for (int i = tid; i < nblk; i += kThreads) {
-    const int64_t x = x0 + i;
-    int lo = 0, hi = P.n_seqs - 1;          // last b with prefix[b] <= x
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
+    const int x = x0 + i;
+    int bq = cseq;
+    if (bq < 0) {
+      int lo = 0, hi = P.n_seqs - 1;        // last b with prefix[b] <= x
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
+      }
+      bq = lo;
     }
-    const int s = P.seq_begin + lo;
-    const SeqBlocks sb = seq_blocks(d, P.layer, s);
     int32_t page;
-    blk_id[i] = block_at(d, s, sb, (int)(x - prefix[lo]), &page);
+    blk_id[i] = block_at(d, P.seq_begin + bq, seqb[bq], x - prefix[bq], &page);
     blk_page[i] = page;
-    blk_seq[i] = lo;
+    blk_seq[i] = bq;
   }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -514,8 +542,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   float* lgbase = LSMEM ? lg_smem : d.logit_scratch + (size_t)c * P.cap * HQ * kBlock;
   const size_t lay_slot = (size_t)P.layer * d.slot_layer_elems;
   float* partials = d.partials;
-  int32_t* arrive = d.counters;
-  int32_t* depart = d.counters + d.max_seqs;
+  int32_t* const ctr_base = d.counters;     // sequence s: arrivals [s * kCounterInts], departures + kDepartAt
 
   // ================================================================ producer warp
   if (warp == kNCW) {
@@ -551,6 +578,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         i0 = i1;
       }
     }
+    __syncwarp();                               // lanes 1..31 wait for the issuing lane
   } else {
     // ============================================================== consumer warps
     const int kvh = warp % HKV, sub = warp / HKV;
@@ -561,7 +589,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       int i1 = i0 + 1;
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
       const int b = blk_seq[i0], s = P.seq_begin + b;
-      const SeqBlocks sb = seq_blocks(d, P.layer, s);
+      const SeqBlocks sb = seqb[b];
 
       // Q fragments of head kvh*8 + g (B operand of QK^T)
       uint32_t qf[8][2];
@@ -656,42 +684,46 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             for (int rr = 0; rr < 4; ++rr) o[mb][rr] += obuf[(kvh * 32 + mb * 4 + rr) * 32 + lane];
         }
         const float ofold = FP8 ? 1.0f / kVFold : 1.0f;
-        float* rec = partials + (size_t)(c + b) * HQ * REC;
+        float* rec = partials + (size_t)(c + b) * HQ * kD;
         const int ha = kvh * kG + 2 * t;
         if constexpr (FP8) {
           // accumulator rows g, g+8 of tile mb hold dims 16g + 2mb and 16g + 2mb + 1:
           // this thread owns dims 16g .. 16g+15 of heads ha and ha+1 (four 16-byte rows)
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            float* ra = rec + (size_t)ha * REC + 4 + 16 * g + 4 * j;
+            float* ra = rec + (size_t)ha * kD + 16 * g + 4 * j;
             *reinterpret_cast<float4*>(ra) = make_float4(o[2 * j][0] * ofold, o[2 * j][2] * ofold,
                                                          o[2 * j + 1][0] * ofold, o[2 * j + 1][2] * ofold);
-            *reinterpret_cast<float4*>(ra + REC) = make_float4(o[2 * j][1] * ofold, o[2 * j][3] * ofold,
-                                                               o[2 * j + 1][1] * ofold, o[2 * j + 1][3] * ofold);
+            *reinterpret_cast<float4*>(ra + kD) = make_float4(o[2 * j][1] * ofold, o[2 * j][3] * ofold,
+                                                              o[2 * j + 1][1] * ofold, o[2 * j + 1][3] * ofold);
           }
         } else {
 #pragma unroll
           for (int mb = 0; mb < 8; ++mb) {
             const int da = 16 * mb + g, db = da + 8;   // dims of accumulator rows g and g+8
-            rec[(size_t)ha * REC + 4 + da] = o[mb][0];
-            rec[(size_t)(ha + 1) * REC + 4 + da] = o[mb][1];
-            rec[(size_t)ha * REC + 4 + db] = o[mb][2];
-            rec[(size_t)(ha + 1) * REC + 4 + db] = o[mb][3];
+            rec[(size_t)ha * kD + da] = o[mb][0];
+            rec[(size_t)(ha + 1) * kD + da] = o[mb][1];
+            rec[(size_t)ha * kD + db] = o[mb][2];
+            rec[(size_t)(ha + 1) * kD + db] = o[mb][3];
           }
         }
+        // (m, l) of each head as one 64-bit word, in a compact array of its own
         if (lane < kG) {
           const int h = kvh * kG + lane;
           float l = lbuf[h];
           for (int w = 1; w < WPK; ++w) l += lbuf[w * HQ + h];
-          rec[(size_t)h * REC + 0] = mseg[h];
-          rec[(size_t)h * REC + 1] = l;
+          d.part_ml[(size_t)(c + b) * HQ + h] = ((unsigned long long)__float_as_uint(l) << 32) | __float_as_uint(mseg[h]);
         }
       }
       named_sync(1, kNCW * 32);
-      // release: the CTA barrier orders every writer's records before this fence
+      // release: the CTA barrier orders every writer's rows and words before this fence.
+      // The arrival order is needed only when nobody waits (spin_limit < 0); otherwise the
+      // increment goes out without a return value.  One poller per CTA reads the counter
+      // (every thread polling the records themselves floods their few L2 lines).
       if (tid == 0) {
         __threadfence();
-        ticket[i0] = atomicAdd(&arrive[s], 1);
+        if (d.spin_limit < 0) ticket[i0] = atomicAdd(ctr_base + (size_t)s * kCounterInts, 1);
+        else red_add(ctr_base + (size_t)s * kCounterInts, 1);
       }
       i0 = i1;
     }
@@ -702,7 +734,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       int i1 = i0 + 1;
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
       const int b = blk_seq[i0], s = P.seq_begin + b;
-      const SeqBlocks sb = seq_blocks(d, P.layer, s);
+      const SeqBlocks sb = seqb[b];
       int cf, cl;                                  // the sequence's CTAs
       if (X > 0) {
         cf = cst[b];
@@ -714,102 +746,159 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const int S = cl - cf + 1;
       if (tid == 0) {
         // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
-        const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1 : wait_at_least(&arrive[s], S, d.spin_limit);
-        __threadfence();
+        const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1
+                                         : wait_at_least(ctr_base + (size_t)s * kCounterInts, S, d.spin_limit);
         flag[0] = ok ? 1 : 0;
         if (!ok) set_error(d, kErrTimeout);
       }
       named_sync(1, kNCW * 32);
       if (!flag[0]) break;
 
-      // global normaliser of every head: rounds of kSC partial records loaded at once;
-      // with S <= kSC the records stay in pm / pl and become the output factors
-      float runM = -INFINITY, runL = 0.f, mown = -INFINITY;
-      for (int c0 = cf; c0 <= cl; c0 += kSC) {
-        const int nc = min(kSC, cl - c0 + 1);
-        for (int idx = tid; idx < nc * HQ; idx += kNCW * 32) {
-          const float* rp = partials + ((size_t)(c0 + idx / HQ + b) * HQ + idx % HQ) * REC;
-          pm[idx] = __ldcg(rp);
-          pl[idx] = __ldcg(rp + 1);
+      // global normaliser: warp w takes heads w, w + 8, ...; lane k reads the (m, l)
+      // word of record k (rounds of 32 records when S > 32); with S <= kSC the
+      // per-record output factors stay in pm
+      {
+        constexpr int HPW = HQ / kNCW;
+        float M[HPW], Ls[HPW], mk[HPW], mo[HPW];
+#pragma unroll
+        for (int u = 0; u < HPW; ++u) { M[u] = -INFINITY; Ls[u] = 0.f; mk[u] = -INFINITY; mo[u] = -INFINITY; }
+        for (int k0 = 0; k0 < S; k0 += 32) {
+          const int k = k0 + lane;
+          // every lane loads (lanes past S re-read record S-1 and ignore it), all loads
+          // issued before any is used
+          const unsigned long long* wp = d.part_ml + (size_t)(cf + min(k, S - 1) + b) * HQ + warp;
+          unsigned long long w[HPW];
+#pragma unroll
+          for (int u = 0; u < HPW; ++u) w[u] = __ldcg(wp + u * kNCW);
+          const int own = c - cf - k0;
+#pragma unroll
+          for (int u = 0; u < HPW; ++u) {
+            const float m = k < S ? __uint_as_float((uint32_t)w[u]) : -INFINITY;
+            const float l = k < S ? __uint_as_float((uint32_t)(w[u] >> 32)) : 0.f;
+            float cm = m;
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+            const float nm = fmaxf(M[u], cm);
+            float part = l * exp2f(m - nm);              // 0 for lanes past S
+#pragma unroll
+            for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+            Ls[u] = Ls[u] * exp2f(M[u] - nm) + part;
+            M[u] = nm;
+            mk[u] = m;
+            if (own >= 0 && own < 32) mo[u] = __shfl_sync(0xffffffffu, m, own);
+          }
         }
-        named_sync(1, kNCW * 32);
-        if (tid < HQ) {
-          float cm = runM;
-          for (int k = 0; k < nc; ++k) cm = fmaxf(cm, pm[k * HQ + tid]);
-          float l = runL * exp2f(runM - cm);
-          for (int k = 0; k < nc; ++k) l += pl[k * HQ + tid] * exp2f(pm[k * HQ + tid] - cm);
-          runM = cm;
-          runL = l;
-          if (c >= c0 && c < c0 + nc) mown = pm[(c - c0) * HQ + tid];
+#pragma unroll
+        for (int u = 0; u < HPW; ++u) {
+          const int h = warp + u * kNCW;
+          const float inv = 1.0f / Ls[u];
+          if (S <= kSC && lane < S) pm[lane * HQ + h] = exp2f(mk[u] - M[u]) * inv;
+          if (lane == 0) {
+            cfac[h] = exp2f(mo[u] - M[u]) * inv;
+            gmax[h] = M[u];
+            ginv[h] = inv;
+          }
         }
-        if (c0 + kSC <= cl) named_sync(1, kNCW * 32);       // pm / pl are reloaded
-      }
-      if (tid < HQ) {
-        cfac[tid] = exp2f(mown - runM) / runL;
-        gmax[tid] = runM;
-        ginv[tid] = 1.0f / runL;
       }
       named_sync(1, kNCW * 32);
       const bool fac_in_smem = S <= kSC;
-      if (fac_in_smem)
-        for (int idx = tid; idx < S * HQ; idx += kNCW * 32) pm[idx] = exp2f(pm[idx] - gmax[idx % HQ]) * ginv[idx % HQ];
-      named_sync(1, kNCW * 32);
 
       if (warp < kNCW / 2) {
-        // masses: one warp per block
+        // masses, one warp per block: lane = (position chunk c4 = lane & 3, head group
+        // hg = lane >> 2 with heads hg, hg + 8, ...), 16-byte reads of the weights
+        const int c4 = lane & 3, hg = lane >> 2;
         for (int i = i0 + warp; i < i1; i += kNCW / 2) {
           float bm = 0.f;                                   // block: max over heads
           for (int h = lane; h < HQ; h += 32) bm = fmaxf(bm, bsum[i * HQ + h] * cfac[h]);
+          float4 tau = make_float4(0.f, 0.f, 0.f, 0.f);     // entry: sum over heads
+#pragma unroll
+          for (int u = 0; u < HQ / 8; ++u) {
+            const int h = hg + 8 * u;
+            const float f = cfac[h];
+            const float4 v = *reinterpret_cast<const float4*>(lgbase + (size_t)(i * HQ + h) * kBlock +
+                                                              (((c4 ^ (h >> 1)) & 3) << 2));
+            tau.x += v.x * f;
+            tau.y += v.y * f;
+            tau.z += v.z * f;
+            tau.w += v.w * f;
+          }
+#pragma unroll
+          for (int o2 = 4; o2 < 32; o2 <<= 1) {
+            tau.x += __shfl_xor_sync(0xffffffffu, tau.x, o2);
+            tau.y += __shfl_xor_sync(0xffffffffu, tau.y, o2);
+            tau.z += __shfl_xor_sync(0xffffffffu, tau.z, o2);
+            tau.w += __shfl_xor_sync(0xffffffffu, tau.w, o2);
+          }
 #pragma unroll
           for (int o2 = 16; o2 > 0; o2 >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
-          const int j = lane & 15, hh = (lane >> 4) * (HQ / 2);
-          float tau = 0.f;                                  // entry: sum over heads
-#pragma unroll 8
-          for (int h = hh; h < hh + HQ / 2; ++h) tau += lgbase[lidx<HQ>(i, h, j)] * cfac[h];
-          tau += __shfl_xor_sync(0xffffffffu, tau, 16);
-          const int64_t p = (int64_t)blk_id[i] * kBlock + j;
-          if (lane < 16 && p >= sb.lo && p < sb.next)       // slot of position p = p % 16
-            d.tok_mass[lay_slot + (size_t)blk_page[i] * kBlock + j] = tau;
+          if (lane < 4) {                                   // positions 4*lane .. +3, slots p % 16
+            const int64_t p0 = (int64_t)blk_id[i] * kBlock + 4 * lane;
+            float* dst = d.tok_mass + lay_slot + (size_t)blk_page[i] * kBlock + 4 * lane;
+            if (p0 >= sb.lo && p0 + 3 < sb.next) {
+              *reinterpret_cast<float4*>(dst) = tau;
+            } else {
+              if (p0 >= sb.lo && p0 < sb.next) dst[0] = tau.x;
+              if (p0 + 1 >= sb.lo && p0 + 1 < sb.next) dst[1] = tau.y;
+              if (p0 + 2 >= sb.lo && p0 + 2 < sb.next) dst[2] = tau.z;
+              if (p0 + 3 >= sb.lo && p0 + 3 < sb.next) dst[3] = tau.w;
+            }
+          }
           if (lane == 0)
             d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
         }
       } else {
-        // output: this CTA combines heads h with h % S == its rank among the sequence's CTAs
+        // output: this CTA combines heads h with h % S == its rank among the sequence's
+        // CTAs, 4 dimensions per thread
+        constexpr int D4 = kD / 4;
+        constexpr size_t kRec4 = (size_t)HQ * kD / 4;      // float4 between a head's records
         const int rank = c - cf;
         const int nh = rank < HQ ? (HQ - rank + S - 1) / S : 0;
         const int ot = tid - (kNCW / 2) * 32;
-        for (int idx = ot; idx < nh * kD; idx += (kNCW / 2) * 32) {
-          const int h = rank + (idx / kD) * S, dd = idx % kD;
-          const float* r0 = partials + ((size_t)(cf + b) * HQ + h) * REC + 4 + dd;
-          float acc = 0.f;
+        for (int idx = ot; idx < nh * D4; idx += (kNCW / 2) * 32) {
+          const int h = rank + (idx / D4) * S, d4 = idx % D4;
+          const float4* r0 = reinterpret_cast<const float4*>(partials + ((size_t)(cf + b) * HQ + h) * kD) + d4;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
           if (fac_in_smem) {
-            for (int k0 = 0; k0 < S; k0 += 16) {                      // 16 loads in flight
-              float ov[16];
+            for (int k0 = 0; k0 < S; k0 += 16) {
+              // 16 unconditional loads in flight (indices past S re-read record S-1,
+              // which then gets factor 0)
+              float4 ov[16];
 #pragma unroll
-              for (int u = 0; u < 16; ++u) ov[u] = (k0 + u < S) ? __ldcg(r0 + (size_t)(k0 + u) * HQ * REC) : 0.f;
+              for (int u = 0; u < 16; ++u) ov[u] = __ldcg(r0 + (size_t)min(k0 + u, S - 1) * kRec4);
 #pragma unroll
-              for (int u = 0; u < 16; ++u)
-                if (k0 + u < S) acc += ov[u] * pm[(k0 + u) * HQ + h];
+              for (int u = 0; u < 16; ++u) {
+                const float f = (k0 + u < S) ? pm[min(k0 + u, S - 1) * HQ + h] : 0.f;
+                acc.x += ov[u].x * f;
+                acc.y += ov[u].y * f;
+                acc.z += ov[u].z * f;
+                acc.w += ov[u].w * f;
+              }
             }
           } else {
-            const float M = gmax[h];
+            const float M = gmax[h], inv = ginv[h];
             for (int k = 0; k < S; ++k) {
-              const float* rp = partials + ((size_t)(cf + k + b) * HQ + h) * REC;
-              acc += __ldcg(rp + 4 + dd) * exp2f(__ldcg(rp) - M);
+              const float f = exp2f(__uint_as_float((uint32_t)__ldcg(d.part_ml + (size_t)(cf + k + b) * HQ + h)) - M);
+              const float4 v = __ldcg(r0 + (size_t)k * kRec4);
+              acc.x += v.x * f;
+              acc.y += v.y * f;
+              acc.z += v.z * f;
+              acc.w += v.w * f;
             }
-            acc *= ginv[h];
+            acc.x *= inv;
+            acc.y *= inv;
+            acc.z *= inv;
+            acc.w *= inv;
           }
-          P.out[((size_t)b * HQ + h) * kD + dd] = acc;
+          reinterpret_cast<float4*>(P.out + ((size_t)b * HQ + h) * kD)[d4] = acc;
         }
       }
-      named_sync(1, kNCW * 32);
-      if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(&depart[s], 1) == S - 1) {   // last CTA of the sequence to leave
-          arrive[s] = 0;
-          depart[s] = 0;
-          __threadfence();
-        }
+      // Departure: once all S CTAs have departed, all have passed the wait and the last
+      // one resets the counters.  (Issuing the departure right after the normaliser and
+      // looking at its ticket only here measured 50% slower in graphs of launches.)
+      named_sync(1, kNCW * 32);                    // also: the next segment reuses pm, cfac, flag
+      if (tid == 0 && atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == S - 1) {
+        ctr_base[(size_t)s * kCounterInts] = 0;    // last CTA of the sequence to leave
+        ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
       }
       i0 = i1;
     }
@@ -968,13 +1057,15 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 size_t static_scratch_limit() { return kStaticScratchBytes; }
 
-// Bytes of the array one launch uses: records for CTA + sequence index < grid + n_seqs,
-// then 2 * max_seqs counters (indexed by absolute sequence).
-size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* counters_offset) {
-  const size_t rec = (size_t)(grid + n_seqs) * d.Hq * kRec * sizeof(float);
-  const size_t off = (rec + 255) & ~size_t(255);
-  *counters_offset = off;
-  return off + 2 * (size_t)d.max_seqs * sizeof(int32_t);
+// Bytes of the array one launch uses: output rows for records (CTA + sequence index)
+// < grid + n_seqs, then their (m, l) words (from *ml_offset), then the counters of all
+// max_seqs sequences (indexed by absolute sequence), each 256-byte aligned.
+size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* ml_offset) {
+  const size_t records = (size_t)(grid + n_seqs);
+  const size_t off = (records * d.Hq * kD * sizeof(float) + 255) & ~size_t(255);
+  *ml_offset = off;
+  const size_t ctr = (off + records * d.Hq * sizeof(unsigned long long) + 255) & ~size_t(255);
+  return ctr + (size_t)kCounterInts * d.max_seqs * sizeof(int32_t);
 }
 
 // Device address of the array on the current device, looked up once per device (the
@@ -1000,8 +1091,9 @@ cudaError_t static_scratch_address(void** out) {
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                                     int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
                                     int grid, cudaStream_t st) {
-  size_t counters_off = 0;
-  if (static_scratch_need(d, n_seqs, grid, &counters_off) > kStaticScratchBytes) return cudaErrorInvalidValue;
+  size_t ml_off = 0;
+  const size_t need = static_scratch_need(d, n_seqs, grid, &ml_off);
+  if (need > kStaticScratchBytes) return cudaErrorInvalidValue;
   Params P;
   P.layer = layer;
   P.seq_begin = seq_begin;
@@ -1025,8 +1117,10 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   if (e != cudaSuccess) return e;
   Dev dd = d;
   dd.partials = static_cast<float*>(base);
-  dd.counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + counters_off);
-  e = cudaMemsetAsync(dd.counters, 0, 2 * (size_t)d.max_seqs * sizeof(int32_t), st);
+  dd.part_ml = reinterpret_cast<unsigned long long*>(static_cast<unsigned char*>(base) + ml_off);
+  dd.counters = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(base) + need -
+                                           (size_t)kCounterInts * d.max_seqs * sizeof(int32_t));
+  e = cudaMemsetAsync(dd.counters, 0, (size_t)kCounterInts * d.max_seqs * sizeof(int32_t), st);
   if (e != cudaSuccess) return e;
   if (d.Hkv == 4) return fp8 ? launch_one<4, true, true>(tk, tv, dd, P, grid, st) : launch_one<4, false, true>(tk, tv, dd, P, grid, st);
   return fp8 ? launch_one<8, true, true>(tk, tv, dd, P, grid, st) : launch_one<8, false, true>(tk, tv, dd, P, grid, st);

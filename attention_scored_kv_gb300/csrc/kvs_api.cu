@@ -25,7 +25,7 @@ cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
                              cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
 size_t static_scratch_limit();
-size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* counters_offset);
+size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* ml_offset);
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                                     int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
                                     int grid, cudaStream_t st);
@@ -45,7 +45,7 @@ struct Plan {
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
   size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, steps, acc_tickets;
-  size_t partials, counters, logits, err;
+  size_t partials, part_ml, counters, logits, err;
 };
 
 size_t esize(int dt) { return dt == KVS_F32 ? 4 : (dt == KVS_BF16 ? 2 : 1); }
@@ -155,8 +155,9 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->last_blk = take(B * MB * 4);
   p->steps = take(B * 4);
   p->acc_tickets = take(B * 4);
-  p->partials = take(((size_t)kGridMax + B) * Hq * (D + 4) * 4);
-  p->counters = take(2 * B * 4);
+  p->partials = take(((size_t)kGridMax + B) * Hq * D * 4);
+  p->part_ml = take(((size_t)kGridMax + B) * Hq * 8);
+  p->counters = take((size_t)kCounterInts * B * 4);
   p->logits = take(p->logit_elems * 4);
   p->err = take(4);
   p->total = o;
@@ -299,6 +300,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.steps = reinterpret_cast<int32_t*>(w + p.steps);
   d.acc_tickets = reinterpret_cast<int32_t*>(w + p.acc_tickets);
   d.partials = reinterpret_cast<float*>(w + p.partials);
+  d.part_ml = reinterpret_cast<unsigned long long*>(w + p.part_ml);
   d.counters = reinterpret_cast<int32_t*>(w + p.counters);
   d.logit_scratch = reinterpret_cast<float*>(w + p.logits);
   d.logit_scratch_elems = p.logit_elems;
@@ -396,6 +398,8 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   kvs_status st = check_range(ctx, seq_begin, n_seqs);
   if (st != KVS_OK) return st;
   if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
   const int B = ctx->cfg.max_seqs;
   int64_t T_bound = 0;
   for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
@@ -419,6 +423,8 @@ kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t
   kvs_status st = check_range(ctx, seq_begin, n_seqs);
   if (st != KVS_OK) return st;
   if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
   if (ctx->kernel != KVS_KERNEL_TENSOR)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the library-owned exchange area serves the tensor-core attend only");
   const int B = ctx->cfg.max_seqs;

@@ -14,7 +14,8 @@
 //     resident count [max_seqs]; free page stack [num_pages] + top
 //     score tables C/E per token [max_seqs][max_positions] double, stamp int32;
 //     C/E per block [max_seqs][max_blocks] double, stamp int32; steps [max_seqs] int32
-//     attend partials [(grid_max + max_seqs)][Hq][D + 4] float; arrival counters
+//     attend partials: output rows [(grid_max + max_seqs)][Hq][D] float and (m, l) words
+//     [(grid_max + max_seqs)][Hq] u64; arrival counters
 //     logit scratch (the general kernel, and the tensor kernel when logits do not fit
 //     in shared memory); accumulate tickets; the error word.
 #pragma once
@@ -36,6 +37,12 @@ enum : int32_t {
   kErrTimeout = 2,       // a bounded wait ran out
   kErrState = 4,         // missing page / inconsistent state seen on device
 };
+
+// The attend's per-sequence arrival and departure counters each sit on a 128-byte line
+// of their own: every CTA of a sequence polls the arrival count, and counters of
+// several sequences on one line made all pollers and all atomics contend for it.
+constexpr int kCounterInts = 64;
+constexpr int kDepartAt = 32;
 
 struct Dev {
   // shape
@@ -65,8 +72,9 @@ struct Dev {
   double* c_blk; double* e_blk; int32_t* last_blk;   // [max_seqs][max_blocks]
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
-  float* partials;        // [(kGridMax + max_seqs)][Hq][D + 4]
-  int32_t* counters;      // [2][max_seqs] arrivals, departures
+  float* partials;        // [records][Hq][D] partial output rows, records = kGridMax + max_seqs
+  unsigned long long* part_ml;   // [records][Hq] softmax partials (l bits << 32 | m bits)
+  int32_t* counters;      // [max_seqs][kCounterInts]: arrivals at 0, departures at kDepartAt
   float* logit_scratch;   size_t logit_scratch_elems;
   int32_t* err;           // [1]
 };
@@ -130,13 +138,14 @@ __device__ __forceinline__ int32_t ld_acquire(const int32_t* p) {
   return v;
 }
 
-// Poll *p until it reaches target, at most `limit` sleeps (limit 0: one look only).
+// Poll *p until it reaches target: at most `limit` polls after the first (limit 0: one
+// look only), 32 ns apart for the first 64, then 100 ns apart.
 // Returns false when the limit ran out (the caller records kErrTimeout).
 __device__ __forceinline__ bool wait_at_least(const int32_t* p, int32_t target, int32_t limit) {
   for (int32_t it = 0;; ++it) {
     if (ld_acquire(p) >= target) return true;
     if (it >= limit) return false;
-    __nanosleep(100);
+    __nanosleep(it < 64 ? 32 : 100);    // short sleeps first: arrivals are close
   }
 }
 

@@ -67,7 +67,7 @@ __global__ void reset_kernel(Dev d, int seq_begin) {
 }
 
 __global__ void clear_kernel(Dev d) {
-  for (int i = threadIdx.x; i < 2 * d.max_seqs; i += blockDim.x) d.counters[i] = 0;
+  for (int i = threadIdx.x; i < kCounterInts * d.max_seqs; i += blockDim.x) d.counters[i] = 0;
   for (int i = threadIdx.x; i < d.max_seqs; i += blockDim.x) d.acc_tickets[i] = 0;
   for (int i = threadIdx.x; i < d.L * d.max_seqs; i += blockDim.x) d.append_tickets[i] = 0;
   if (threadIdx.x == 0) *d.err = 0;

@@ -153,13 +153,15 @@ KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
 
 /* Decode attention of one query per head over the resident entries of layer `layer`.
  * d_q: [n_seqs][num_q_heads][head_dim] in in_dtype; d_out: [n_seqs][num_q_heads]
- * [head_dim] float32, both device memory.  Logits are q.k/sqrt(D) (k, v decoded
- * inline from E4M3 as code * scale), softmax per head over the resident entries.
+ * [head_dim] float32, both device memory aligned to 16 bytes.  Logits are
+ * q.k/sqrt(D) (k, v decoded inline from E4M3 as code * scale), softmax per head
+ * over the resident entries.
  * In the same launch, without writing the weights anywhere off chip, the kernel
  * stores the step masses of this layer: per resident entry the sum over query heads
  * of its weight, and per resident 16-token block the maximum over query heads of
  * the head's summed weight in the block (both readable with kvs_read_state).
- * Errors: KVS_ERR_EMPTY_CACHE if a sequence of the range has no resident entry. */
+ * Errors: KVS_ERR_EMPTY_CACHE if a sequence of the range has no resident entry;
+ * KVS_ERR_INVALID_ARGUMENT if d_q or d_out is NULL or not 16-byte aligned. */
 KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
                              const void* d_q, float* d_out, kvs_stream_t stream);
 
@@ -181,8 +183,10 @@ KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  *   KVS_ERR_UNSUPPORTED  the context does not use the tensor-core attend, or this
  *                        launch's logits do not fit in shared memory;
  *   KVS_ERR_CAPACITY     the launch needs more than the array holds:
- *                        (grid + n_seqs) * num_q_heads * (head_dim + 2) * 4 bytes,
- *                        rounded up to 256, plus 8 * max_seqs bytes must be <= 8 MiB.
+ *                        (grid + n_seqs) * num_q_heads * head_dim * 4 bytes,
+ *                        rounded up to 256, plus (grid + n_seqs) * num_q_heads * 8
+ *                        rounded up to 256, plus 256 * max_seqs bytes must be
+ *                        <= 8 MiB.
  * The array is shared by every call of every context on the device and keeps the last
  * call's contents; the counters are cleared on `stream` before each launch.  Two such
  * launches that overlap on the GPU (different streams or contexts) race on the array:

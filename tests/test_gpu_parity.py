@@ -58,6 +58,10 @@ SMALL = {
                                        retrieval_pos=500, steps=6, prefill_chunk=0),
     "e4m3-h2o": workloads.scaled_down("e4m3-b64-ragged-h2o2048", num_layers=2, batch=5, context_range=(100, 700),
                                       h2o_budget_tokens=256, steps=40, prefill_chunk=256),
+    # 16 sequences of 65 resident blocks: several blocks per CTA and about 9 CTAs per
+    # sequence, the shape of the 32K-context batch at a smaller window
+    "e4m3-b16-window": workloads.scaled_down("e4m3-b16-ctx32768-window4096", num_layers=2, batch=16,
+                                             context=2500, window=1024, steps=6, prefill_chunk=512),
 }
 
 
