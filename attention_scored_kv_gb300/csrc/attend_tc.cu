@@ -804,36 +804,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const bool fac_in_smem = S <= kSC;
 
       if (warp < kNCW / 2) {
-        // masses, one warp per block: lane = (position chunk c4 = lane & 3, head group
-        // hg = lane >> 2 with heads hg, hg + 8, ...), 16-byte reads of the weights
-        const int c4 = lane & 3, hg = lane >> 2;
-        for (int i = i0 + warp; i < i1; i += kNCW / 2) {
-          float bm = 0.f;                                   // block: max over heads
-          for (int h = lane; h < HQ; h += 32) bm = fmaxf(bm, bsum[i * HQ + h] * cfac[h]);
-          float4 tau = make_float4(0.f, 0.f, 0.f, 0.f);     // entry: sum over heads
-#pragma unroll
-          for (int u = 0; u < HQ / 8; ++u) {
-            const int h = hg + 8 * u;
-            const float f = cfac[h];
-            const float4 v = *reinterpret_cast<const float4*>(lgbase + (size_t)(i * HQ + h) * kBlock +
-                                                              (((c4 ^ (h >> 1)) & 3) << 2));
-            tau.x += v.x * f;
-            tau.y += v.y * f;
-            tau.z += v.z * f;
-            tau.w += v.w * f;
-          }
-#pragma unroll
-          for (int o2 = 4; o2 < 32; o2 <<= 1) {
-            tau.x += __shfl_xor_sync(0xffffffffu, tau.x, o2);
-            tau.y += __shfl_xor_sync(0xffffffffu, tau.y, o2);
-            tau.z += __shfl_xor_sync(0xffffffffu, tau.z, o2);
-            tau.w += __shfl_xor_sync(0xffffffffu, tau.w, o2);
-          }
-#pragma unroll
-          for (int o2 = 16; o2 > 0; o2 >>= 1) bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o2));
-          if (lane < 4) {                                   // positions 4*lane .. +3, slots p % 16
-            const int64_t p0 = (int64_t)blk_id[i] * kBlock + 4 * lane;
-            float* dst = d.tok_mass + lay_slot + (size_t)blk_page[i] * kBlock + 4 * lane;
+        // masses: lane = (block bi = lane >> 2 of 8 per warp round, position chunk
+        // c4 = lane & 3); each lane walks all heads for its 4 positions (no shuffles),
+        // block bi starting at head bi so that the 16-byte reads of one quarter-warp
+        // cover all banks
+        const int bi = lane >> 2, c4 = lane & 3;
+        for (int ib = i0 + warp * 8; ib < i1; ib += (kNCW / 2) * 8) {
+          const int i = ib + bi;
+          if (i < i1) {
+            const float* lgi = lgbase + (size_t)i * HQ * kBlock;
+            const float* bsi = bsum + i * HQ;
+            float4 tau = make_float4(0.f, 0.f, 0.f, 0.f);   // entry: sum over heads
+            float bm = 0.f;                                 // block: max over heads
+#pragma unroll 8
+            for (int u = 0; u < HQ; ++u) {
+              const int h = (u + bi) & (HQ - 1);
+              const float f = cfac[h];
+              const float4 v = *reinterpret_cast<const float4*>(lgi + h * kBlock + (((c4 ^ (h >> 1)) & 3) << 2));
+              tau.x += v.x * f;
+              tau.y += v.y * f;
+              tau.z += v.z * f;
+              tau.w += v.w * f;
+              bm = fmaxf(bm, bsi[h] * f);
+            }
+            const int64_t p0 = (int64_t)blk_id[i] * kBlock + 4 * c4;   // slots p % 16
+            float* dst = d.tok_mass + lay_slot + (size_t)blk_page[i] * kBlock + 4 * c4;
             if (p0 >= sb.lo && p0 + 3 < sb.next) {
               *reinterpret_cast<float4*>(dst) = tau;
             } else {
@@ -842,9 +837,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
               if (p0 + 2 >= sb.lo && p0 + 2 < sb.next) dst[2] = tau.z;
               if (p0 + 3 >= sb.lo && p0 + 3 < sb.next) dst[3] = tau.w;
             }
+            if (c4 == 0)
+              d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
           }
-          if (lane == 0)
-            d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
         }
       } else {
         // output: this CTA combines heads h with h % S == its rank among the sequence's
