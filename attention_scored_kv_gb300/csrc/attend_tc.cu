@@ -338,6 +338,12 @@ struct Params {
   const void* q;                       // [n_seqs][HQ][D] bf16
   float* out;                          // [n_seqs][HQ][D]
   float qk_scale;                      // log2(e) / sqrt(D)
+  // Whole-CTA plan made on the host from the per-sequence block bounds (whole > 0):
+  // sequence b owns CTAs [cst[b], cst[b+1]) and splits its blocks evenly over them.
+  // The bounds hold for every later state the launch can see (a graph replays it), so
+  // the plan stays valid; whole == 0 leaves the split to the device.
+  int whole;
+  int cst[kGridMax + 1];
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
@@ -359,7 +365,7 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   p.bars = o;   o += (size_t)2 * ns * 8;
   p.seqb = o;   o = up16(o + (size_t)n_seqs * sizeof(SeqBlocks));
   p.blk = o;    o = up16(o + (size_t)4 * cap * 4);
-  p.prefix = o; o = up16(o + (size_t)2 * (n_seqs + 1) * 4);    // prefix, then cst
+  p.prefix = o; o = up16(o + (size_t)(n_seqs + 1) * 4);
   p.mbuf = o;   o += (size_t)WPK * HQ * 4;
   p.lbuf = o;   o += (size_t)WPK * HQ * 4;
   p.hv = o;     o += (size_t)4 * HQ * 4;
@@ -394,7 +400,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   int32_t* blk_seq = blk_page + P.cap;
   int32_t* ticket = blk_seq + P.cap;                                   // arrival order, by segment start
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + sp.prefix);       // [n_seqs + 1]
-  int32_t* cst = prefix + P.n_seqs + 1;                                 // [n_seqs + 1]
   float* mbuf = reinterpret_cast<float*>(smem + sp.mbuf);              // [WPK][HQ]
   float* lbuf = reinterpret_cast<float*>(smem + sp.lbuf);              // [WPK][HQ]
   float* mseg = reinterpret_cast<float*>(smem + sp.hv);                // [HQ]
@@ -412,99 +417,59 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   const int c = blockIdx.x, G = gridDim.x;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
 
-  // ---------------------------------------------------------------- partition
-  if (warp == 0) {
-    int run = 0;
-    for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
-      const int b = b0 + lane;
-      int nb = 0;
-      if (b < P.n_seqs) {
-        const SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
-        seqb[b] = sb;
-        nb = sb.n;
-      }
-      int incl = nb;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (b < P.n_seqs) prefix[b] = run + incl - nb;
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    if (lane == 0) prefix[P.n_seqs] = run;
-    __syncwarp();
-    // Whole CTAs per sequence: with X blocks per CTA at most, sequence b takes
-    // ceil(n_b / X) CTAs; any X whose total is at most G will do.  Each CTA then holds
-    // one segment (one flush, one combine), so no CTA does two sequences' work in
-    // series.  X starts from an estimate that leaves half a CTA of slack per sequence;
-    // the split falls back to blocks end to end when no X within the per-CTA capacity
-    // fits.  ctas_for leaves each sequence's count in cst[].
-    int X = 0;
-    if (P.n_seqs <= G && run > 0) {
-      auto ctas_for = [&](int x) {
-        int cnt = 0;
-        for (int b = lane; b < P.n_seqs; b += 32) {
-          const int cb = (prefix[b + 1] - prefix[b] + x - 1) / x;
-          cst[b] = cb;
-          cnt += cb;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(0xffffffffu, cnt, o);
-        return cnt;
-      };
-      const int lo = (run + G - 1) / G, hi = P.cap;
-      int x = (2 * run + (2 * G - P.n_seqs) - 1) / (2 * G - P.n_seqs);   // ceil(T / (G - n/2))
-      if (x < lo) x = lo;
-      for (int it = 0; it < 3 && x < hi; ++it) {
-        if (ctas_for(x) <= G) { X = x; break; }
-        x += 1 + x / 16;
-      }
-      if (X == 0 && lo <= hi && ctas_for(hi) <= G) X = hi;
-      __syncwarp();
-      if (X > 0) {
-        int crun = 0;
-        for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
-          const int b = b0 + lane;
-          const int cb = b < P.n_seqs ? cst[b] : 0;
-          int incl = cb;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          __syncwarp();
-          if (b < P.n_seqs) cst[b] = crun + incl - cb;
-          crun += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) cst[P.n_seqs] = crun;
-      }
-    }
-    if (lane == 0) flag[1] = X;
+  if (warp == kNCW && lane == 0) {          // fetch the two tensor maps before the first copy
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
-  __syncthreads();
-  const int X = flag[1];
-  const int T = prefix[P.n_seqs];
-  const int q = T / G, r = T % G;
-  int x0 = 0;
-  int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole-CTA split)
-  if (X > 0) {
-    // sequence b owns CTAs [cst[b], cst[b+1]); its blocks are split evenly over them
-    if (c < cst[P.n_seqs]) {
+
+  // ---------------------------------------------------------------- partition
+  int x0 = 0;                               // whole plan: block index within the sequence
+  int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole plan)
+  int q = 0, r = 0;                         // device split: T = q * G + r
+  SeqBlocks sbw = {};                       // whole plan: the CTA's sequence
+  if (P.whole) {
+    if (c < P.cst[P.n_seqs]) {
       int lo = 0, hi = P.n_seqs - 1;        // last b with cst[b] <= c
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (cst[mid] <= c) lo = mid; else hi = mid - 1;
+        if (P.cst[mid] <= c) lo = mid; else hi = mid - 1;
       }
-      const int S = cst[lo + 1] - cst[lo], rk = c - cst[lo];
-      const int nb = prefix[lo + 1] - prefix[lo], qb = nb / S, rb = nb % S;
-      x0 = prefix[lo] + rk * qb + (rk < rb ? rk : rb);
+      sbw = seq_blocks(d, P.layer, P.seq_begin + lo);
+      const int cb = P.cst[lo + 1] - P.cst[lo], rk = c - P.cst[lo];
+      const int qb = sbw.n / cb, rb = sbw.n % cb;
+      x0 = rk * qb + (rk < rb ? rk : rb);
       nblk = qb + (rk < rb ? 1 : 0);
       cseq = lo;
+      if (tid == 0) seqb[lo] = sbw;
     }
   } else {
+    if (warp == 0) {
+      int run = 0;
+      for (int b0 = 0; b0 < P.n_seqs; b0 += 32) {
+        const int b = b0 + lane;
+        int nb = 0;
+        if (b < P.n_seqs) {
+          const SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
+          seqb[b] = sb;
+          nb = sb.n;
+        }
+        int incl = nb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += v;
+        }
+        if (b < P.n_seqs) prefix[b] = run + incl - nb;
+        run += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) prefix[P.n_seqs] = run;
+    }
+    __syncthreads();
     // CTA c takes q + (c < r) consecutive blocks (T = q*G + r): no empty CTA ever sits
     // between two non-empty ones, so a sequence's CTAs are a gap-free range.
+    const int T = prefix[P.n_seqs];
+    q = T / G;
+    r = T % G;
     x0 = c * q + (c < r ? c : r);
     nblk = q + (c < r ? 1 : 0);
   }
@@ -512,21 +477,26 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     if (tid == 0) set_error(d, kErrCapacity);
     return;
   }
-  for (int i = tid; i < nblk; i += kThreads) {
-    const int x = x0 + i;
-    int bq = cseq;
-    if (bq < 0) {
+  if (cseq >= 0) {
+    for (int i = tid; i < nblk; i += kThreads) {
+      int32_t page;
+      blk_id[i] = block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+      blk_page[i] = page;
+      blk_seq[i] = cseq;
+    }
+  } else {
+    for (int i = tid; i < nblk; i += kThreads) {
+      const int x = x0 + i;
       int lo = 0, hi = P.n_seqs - 1;        // last b with prefix[b] <= x
       while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
       }
-      bq = lo;
+      int32_t page;
+      blk_id[i] = block_at(d, P.seq_begin + lo, seqb[lo], x - prefix[lo], &page);
+      blk_page[i] = page;
+      blk_seq[i] = lo;
     }
-    int32_t page;
-    blk_id[i] = block_at(d, P.seq_begin + bq, seqb[bq], x - prefix[bq], &page);
-    blk_page[i] = page;
-    blk_seq[i] = bq;
   }
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) {
@@ -735,15 +705,15 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
       const int b = blk_seq[i0], s = P.seq_begin + b;
       const SeqBlocks sb = seqb[b];
-      int cf, cl;                                  // the sequence's CTAs
-      if (X > 0) {
-        cf = cst[b];
-        cl = cst[b + 1] - 1;
+      int cf, S;                                   // the sequence's CTAs: cf .. cf + S - 1
+      if (P.whole) {
+        const int cb = P.cst[b + 1] - P.cst[b];
+        cf = P.cst[b];
+        S = sb.n >= cb ? cb : sb.n;                // fewer blocks than CTAs: one block each
       } else {
         cf = cta_of(prefix[b], q, r);
-        cl = cta_of(prefix[b + 1] - 1, q, r);
+        S = cta_of(prefix[b + 1] - 1, q, r) - cf + 1;
       }
-      const int S = cl - cf + 1;
       if (tid == 0) {
         // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
         const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1
@@ -940,18 +910,45 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
   return cudaLaunchKernelEx(&cfg, fn, tk, tv, d, P);
 }
 
-// Per-CTA block capacity that leaves the partition room to give every sequence whole
-// CTAs (up to an eighth more blocks than an even split, plus two).
+// Per-CTA block capacity a whole-CTA plan may use: up to an eighth more blocks than an
+// even split, plus two.
 int wide_cap(int base) { return base + base / 8 + 2; }
+
+// Whole CTAs per sequence, planned on the host from the per-sequence block bounds: the
+// fewest blocks per CTA X <= cap_limit such that ceil(bound_b / X) CTAs for every
+// sequence b take at most `grid` CTAs.  Fills P.cst, sets P.whole and P.cap = X; false
+// (P unchanged) when no such X exists or the launch has more sequences than CTAs.
+bool plan_whole(Params& P, const int32_t* bounds, int grid, int cap_limit) {
+  if (P.n_seqs > grid || P.n_seqs > kGridMax) return false;
+  int64_t T = 0;
+  for (int b = 0; b < P.n_seqs; ++b) T += bounds[b] > 0 ? bounds[b] : 0;
+  if (T <= 0) return false;
+  auto ctas = [&](int x) {
+    int64_t n = 0;
+    for (int b = 0; b < P.n_seqs; ++b) n += (bounds[b] + x - 1) / x;
+    return n;
+  };
+  int lo = (int)((T + grid - 1) / grid), hi = cap_limit;
+  if (lo < 1) lo = 1;
+  if (lo > hi || ctas(hi) > grid) return false;
+  while (lo < hi) {
+    const int mid = (lo + hi) / 2;
+    if (ctas(mid) <= grid) hi = mid; else lo = mid + 1;
+  }
+  int run = 0;
+  for (int b = 0; b < P.n_seqs; ++b) {
+    P.cst[b] = run;
+    run += (bounds[b] + lo - 1) / lo;
+  }
+  P.cst[P.n_seqs] = run;
+  P.whole = 1;
+  P.cap = lo;
+  return true;
+}
 
 template <int HKV, bool FP8>
 cudaError_t launch_pick(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, Params P, int grid,
                         cudaStream_t st) {
-  const int base = P.cap;
-  P.cap = wide_cap(base);                  // room for whole CTAs per sequence
-  P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
-  if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
-  P.cap = base;
   P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
   if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
   P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs);
@@ -996,21 +993,33 @@ cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int
 int tc_cap(int64_t T_bound, int grid) { return (int)((T_bound + grid - 1) / grid); }
 
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                             int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound, int grid,
-                             cudaStream_t st) {
+                             int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
+                             int grid, cudaStream_t st) {
   Params P;
   P.layer = layer;
   P.seq_begin = seq_begin;
   P.n_seqs = n_seqs;
-  P.cap = tc_cap(T_bound, grid);
-  if (P.cap < 1) P.cap = 1;
+  int64_t T_bound = 0;
+  for (int b = 0; b < n_seqs; ++b) T_bound += bounds[b];
+  const int cap0 = tc_cap(T_bound, grid) < 1 ? 1 : tc_cap(T_bound, grid);
+  P.cap = cap0;
   P.ns = 0;
   P.q = q;
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
+  P.whole = 0;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
-  if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, P, grid, st) : launch_pick<4, false>(tk, tv, d, P, grid, st);
-  return fp8 ? launch_pick<8, true>(tk, tv, d, P, grid, st) : launch_pick<8, false>(tk, tv, d, P, grid, st);
+  auto pick = [&](const Params& PP) {
+    if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, PP, grid, st) : launch_pick<4, false>(tk, tv, d, PP, grid, st);
+    return fp8 ? launch_pick<8, true>(tk, tv, d, PP, grid, st) : launch_pick<8, false>(tk, tv, d, PP, grid, st);
+  };
+  if (plan_whole(P, bounds, grid, wide_cap(cap0))) {
+    const cudaError_t e = pick(P);
+    if (e != cudaErrorInvalidConfiguration) return e;
+    P.whole = 0;                            // the plan's buffers do not fit: split on the device
+    P.cap = cap0;
+  }
+  return pick(P);
 }
 
 // Largest grid the cooperative launch allows with one CTA per SM.
@@ -1084,7 +1093,7 @@ cudaError_t static_scratch_address(void** out) {
 // cudaErrorNotSupported if its logits do not fit in shared memory (that case needs the
 // workspace's logit scratch).
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                                    int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
+                                    int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
                                     int grid, cudaStream_t st) {
   size_t ml_off = 0;
   const size_t need = static_scratch_need(d, n_seqs, grid, &ml_off);
@@ -1093,19 +1102,24 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   P.layer = layer;
   P.seq_begin = seq_begin;
   P.n_seqs = n_seqs;
-  P.cap = tc_cap(T_bound, grid);
-  if (P.cap < 1) P.cap = 1;
+  int64_t T_bound = 0;
+  for (int b = 0; b < n_seqs; ++b) T_bound += bounds[b];
+  const int cap0 = tc_cap(T_bound, grid) < 1 ? 1 : tc_cap(T_bound, grid);
+  P.cap = cap0;
   P.q = q;
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
+  P.whole = 0;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
-  const int cap0 = P.cap;
-  P.cap = wide_cap(cap0);
-  P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
-  if (P.ns == 0) {
-    P.cap = cap0;
+  P.ns = 0;
+  if (plan_whole(P, bounds, grid, wide_cap(cap0))) {
     P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+    if (P.ns == 0) {
+      P.whole = 0;
+      P.cap = cap0;
+    }
   }
+  if (P.ns == 0) P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
   if (P.ns == 0) return cudaErrorNotSupported;
   void* base = nullptr;
   cudaError_t e = static_scratch_address(&base);

@@ -21,13 +21,13 @@ namespace kvs {
 bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window, int mode);
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                             int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound, int grid,
+                             int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
                              cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
 size_t static_scratch_limit();
 size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* ml_offset);
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                                    int seq_begin, int n_seqs, const void* q, float* out, int64_t T_bound,
+                                    int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
                                     int grid, cudaStream_t st);
 }  // namespace kvs
 
@@ -173,6 +173,7 @@ struct kvs_ctx {
   std::vector<int64_t> next;        // [L][max_seqs]
   std::vector<int64_t> frontier;    // [max_seqs] max over layers of next (pages allocated below it)
   std::vector<int64_t> h2o_bound;   // [max_seqs] bound on resident blocks (H2O)
+  std::vector<int32_t> bounds;      // per-launch scratch: block bound of each sequence
   std::vector<CUtensorMap> maps;    // [L][2]
   std::string err;
 };
@@ -401,16 +402,16 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
   const int B = ctx->cfg.max_seqs;
-  int64_t T_bound = 0;
+  ctx->bounds.resize((size_t)n_seqs);
   for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
     if (ctx->next[(size_t)layer * B + s] == 0)
       return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
-    T_bound += seq_block_bound(ctx, s);
+    ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (ctx->kernel == KVS_KERNEL_TENSOR) {
     return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
-                                         n_seqs, d_q, d_out, T_bound, ctx->grid, cs),
+                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, cs),
                    "tensor-core attend");
   }
   return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
@@ -428,11 +429,11 @@ kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t
   if (ctx->kernel != KVS_KERNEL_TENSOR)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the library-owned exchange area serves the tensor-core attend only");
   const int B = ctx->cfg.max_seqs;
-  int64_t T_bound = 0;
+  ctx->bounds.resize((size_t)n_seqs);
   for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
     if (ctx->next[(size_t)layer * B + s] == 0)
       return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
-    T_bound += seq_block_bound(ctx, s);
+    ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
   }
   size_t off = 0;
   const size_t need = static_scratch_need(ctx->dev, n_seqs, ctx->grid, &off);
@@ -440,7 +441,7 @@ kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t
     return fail(ctx, KVS_ERR_CAPACITY, "this launch needs %zu bytes of exchange area; the library array holds %zu",
                 need, static_scratch_limit());
   const cudaError_t e = launch_attend_tc_static(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
-                                                seq_begin, n_seqs, d_q, d_out, T_bound, ctx->grid,
+                                                seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid,
                                                 reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the logits of this launch do not fit in shared memory");
