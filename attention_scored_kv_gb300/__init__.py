@@ -139,6 +139,21 @@ class KVCache:
                                             _stream(stream)))
         return out
 
+    def append_attend(self, layer, k, v, q, out=None, seq_begin=0, stream=None):
+        """append_kv of one token per sequence then decode_attend, in one launch where
+        the context allows.  k, v: [n_seqs, 1, Hkv, D]; q: [n_seqs, Hq, D]."""
+        _, Hq, Hkv, D = self.shape
+        n_seqs = int(q.shape[0])
+        _need(k, "k", self.in_dtype, (n_seqs, 1, Hkv, D))
+        _need(v, "v", self.in_dtype, (n_seqs, 1, Hkv, D))
+        _need(q, "q", self.in_dtype, (n_seqs, Hq, D))
+        if out is None:
+            out = torch.empty((n_seqs, Hq, D), dtype=torch.float32, device=q.device)
+        _need(out, "out", torch.float32, (n_seqs, Hq, D))
+        self._check(lib().kvs_append_attend(self._ctx, layer, seq_begin, n_seqs, _ptr(k), _ptr(v), _ptr(q),
+                                            _ptr(out), _stream(stream)))
+        return out
+
     def decode_attend_static_scratch(self, layer, q, out=None, seq_begin=0, stream=None):
         """decode_attend with the exchange area in the library's own fixed array instead
         of this cache's workspace (for callers that cannot supply device memory)."""

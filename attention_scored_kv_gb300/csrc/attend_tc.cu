@@ -37,6 +37,7 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include "append_store.cuh"
 #include "kvs_internal.cuh"
 
 namespace kvs {
@@ -344,6 +345,11 @@ struct Params {
   // the plan stays valid; whole == 0 leaves the split to the device.
   int whole;
   int cst[kGridMax + 1];
+  // Fused append (whole plan only): before attending, store one new token per sequence,
+  // K and V rows [n_seqs][Hkv][D] in the input dtype, at position next_position.
+  int fuse;
+  const void* k_new;
+  const void* v_new;
 };
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
@@ -362,7 +368,7 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   size_t o = 0;
   p.ring = o;   o += (size_t)ns * sb * blk;
   p.sscale = o; o += (size_t)ns * sb * kBlock * 4;
-  p.bars = o;   o += (size_t)2 * ns * 8;
+  p.bars = o;   o += (size_t)(2 * ns + 1) * 8;                   // full, empty, append done
   p.seqb = o;   o = up16(o + (size_t)n_seqs * sizeof(SeqBlocks));
   p.blk = o;    o = up16(o + (size_t)4 * cap * 4);
   p.prefix = o; o = up16(o + (size_t)(n_seqs + 1) * 4);
@@ -393,7 +399,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   const SmemPlan sp = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, NS);
   uint8_t* ring = smem + sp.ring;
   float* sscale = reinterpret_cast<float*>(smem + sp.sscale);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.bars);          // full[NS], empty[NS]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.bars);          // full[NS], empty[NS], app
   SeqBlocks* seqb = reinterpret_cast<SeqBlocks*>(smem + sp.seqb);        // [n_seqs]
   int32_t* blk_id = reinterpret_cast<int32_t*>(smem + sp.blk);
   int32_t* blk_page = blk_id + P.cap;
@@ -415,7 +421,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS);
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS), app_bar = smem_u32(bars + 2 * NS);
 
   if (warp == kNCW && lane == 0) {          // fetch the two tensor maps before the first copy
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
@@ -427,6 +433,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole plan)
   int q = 0, r = 0;                         // device split: T = q * G + r
   SeqBlocks sbw = {};                       // whole plan: the CTA's sequence
+  int wseq = -1;                            // whole plan: the sequence whose CTAs include c
+  bool appends = false;                     // fused append: this CTA stores the new token
   if (P.whole) {
     if (c < P.cst[P.n_seqs]) {
       int lo = 0, hi = P.n_seqs - 1;        // last b with cst[b] <= c
@@ -434,12 +442,19 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const int mid = (lo + hi + 1) >> 1;
         if (P.cst[mid] <= c) lo = mid; else hi = mid - 1;
       }
-      sbw = seq_blocks(d, P.layer, P.seq_begin + lo);
+      wseq = lo;
+      int64_t nxt = d.next_pos[(size_t)P.layer * d.max_seqs + P.seq_begin + lo];
+      // fused append: attend over the state after the new position (the host checked the
+      // capacity; a state that disagrees skips the append and reports it)
+      const bool grow = P.fuse && nxt < d.max_positions;
+      if (P.fuse && !grow && tid == 0) set_error(d, kErrCapacity);
+      sbw = seq_blocks_at(d, P.seq_begin + lo, grow ? nxt + 1 : nxt);
       const int cb = P.cst[lo + 1] - P.cst[lo], rk = c - P.cst[lo];
       const int qb = sbw.n / cb, rb = sbw.n % cb;
       x0 = rk * qb + (rk < rb ? rk : rb);
       nblk = qb + (rk < rb ? 1 : 0);
-      cseq = lo;
+      if (nblk > 0) cseq = lo;
+      appends = grow && nblk > 0 && x0 + nblk == sbw.n;   // holds the newest block
       if (tid == 0) seqb[lo] = sbw;
     }
   } else {
@@ -503,16 +518,29 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kNCW);      // every consumer warp releases every stage
     }
+    mbar_init(app_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
   __syncthreads();
-  if (nblk == 0) return;
+  int32_t* const ctr_base = d.counters;     // sequence s: arrivals [s * kCounterInts], departures + kDepartAt
+  if (nblk == 0) {
+    // A CTA of the whole plan with no block still read its sequence's next position:
+    // it departs too, so that the last CTA to leave knows every reader is done.
+    if (wseq >= 0 && tid == 0) {
+      const int s = P.seq_begin + wseq, cb = P.cst[wseq + 1] - P.cst[wseq];
+      if (atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == cb - 1) {
+        ctr_base[(size_t)s * kCounterInts] = 0;
+        ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
+        if (P.fuse && sbw.next > 0) d.next_pos[(size_t)P.layer * d.max_seqs + s] = sbw.next;
+      }
+    }
+    return;
+  }
 
   float* lgbase = LSMEM ? lg_smem : d.logit_scratch + (size_t)c * P.cap * HQ * kBlock;
   const size_t lay_slot = (size_t)P.layer * d.slot_layer_elems;
   float* partials = d.partials;
-  int32_t* const ctr_base = d.counters;     // sequence s: arrivals [s * kCounterInts], departures + kDepartAt
 
   // ================================================================ producer warp
   if (warp == kNCW) {
@@ -530,6 +558,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             const int nb = min(C::SB, i1 - g0);
             const uint32_t st = ctr % NS, round = ctr / NS;
             if (round > 0 && !mbar_wait(empty0 + 8 * st, (round - 1) & 1)) set_error(d, kErrTimeout);
+            // the newest block (the CTA's last) is copied only once the fused append is stored
+            if (appends && g0 + nb == nblk && !mbar_wait(app_bar, 0)) set_error(d, kErrTimeout);
             const uint32_t fb = full0 + 8 * st;
             mbar_expect_tx(fb, nb * (C::BLK + (FP8 ? kBlock * 4 : 0)));
             for (int j = 0; j < nb; ++j) {
@@ -553,6 +583,30 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     // ============================================================== consumer warps
     const int kvh = warp % HKV, sub = warp / HKV;
     const int g = lane >> 2, t = lane & 3;
+    if (appends) {
+      // fused append of position next (the state attended is next + 1): warp 0 stores K,
+      // warp 1 stores V, exactly as the append kernel does; every storing lane orders its
+      // generic-proxy stores before the copies the producer issues after app_bar
+      const int s = P.seq_begin + cseq;
+      const int64_t pnew = sbw.next - 1;
+      if (warp < 2) {
+        int32_t slot;
+        const int32_t page = page_of(d, s, pnew, &slot);
+        const size_t src_elem = (size_t)cseq * d.Hkv * d.D;
+        const size_t lay_slot0 = (size_t)P.layer * d.slot_layer_elems + (size_t)page * kBlock;
+        uint8_t* base = (warp == 0 ? d.k_pages : d.v_pages) + P.layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
+        float* scales = warp == 0 ? d.k_scales : d.v_scales;
+        store_position<FP8 ? KVS_E4M3 : KVS_BF16, KVS_BF16>(d, warp == 0 ? P.k_new : P.v_new, src_elem, base,
+                                                          scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
+        if (warp == 0 && lane == 0) d.pos[lay_slot0 + slot] = pnew;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      named_sync(1, kNCW * 32);
+      if (tid == 0) {
+        __threadfence();
+        mbar_arrive(app_bar);
+      }
+    }
     uint32_t ctr = 0;
     int i0 = 0;
     while (i0 < nblk) {
@@ -861,9 +915,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       // one resets the counters.  (Issuing the departure right after the normaliser and
       // looking at its ticket only here measured 50% slower in graphs of launches.)
       named_sync(1, kNCW * 32);                    // also: the next segment reuses pm, cfac, flag
-      if (tid == 0 && atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == S - 1) {
+      const int departs = P.whole ? P.cst[b + 1] - P.cst[b] : S;   // whole plan: empty CTAs depart too
+      if (tid == 0 && atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == departs - 1) {
         ctr_base[(size_t)s * kCounterInts] = 0;    // last CTA of the sequence to leave
         ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
+        if (P.fuse) d.next_pos[(size_t)P.layer * d.max_seqs + s] = sb.next;   // every reader is done
       }
       i0 = i1;
     }
@@ -992,9 +1048,12 @@ cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int
 // Blocks one CTA must hold for a launch whose resident blocks number at most T_bound.
 int tc_cap(int64_t T_bound, int grid) { return (int)((T_bound + grid - 1) / grid); }
 
+// k_new / v_new non-null: append one token per sequence in the same launch (NONE and
+// WINDOW modes, whole-CTA plan); cudaErrorNotSupported when that plan is not possible
+// or its buffers do not fit.
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                              int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
-                             int grid, cudaStream_t st) {
+                             int grid, const void* k_new, const void* v_new, cudaStream_t st) {
   Params P;
   P.layer = layer;
   P.seq_begin = seq_begin;
@@ -1008,17 +1067,27 @@ cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
   P.whole = 0;
+  P.fuse = 0;
+  P.k_new = P.v_new = nullptr;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
   auto pick = [&](const Params& PP) {
     if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, PP, grid, st) : launch_pick<4, false>(tk, tv, d, PP, grid, st);
     return fp8 ? launch_pick<8, true>(tk, tv, d, PP, grid, st) : launch_pick<8, false>(tk, tv, d, PP, grid, st);
   };
   if (plan_whole(P, bounds, grid, wide_cap(cap0))) {
+    if (k_new) {                            // fused append: whole plan only
+      P.fuse = 1;
+      P.k_new = k_new;
+      P.v_new = v_new;
+      const cudaError_t e = pick(P);
+      return e == cudaErrorInvalidConfiguration ? cudaErrorNotSupported : e;
+    }
     const cudaError_t e = pick(P);
     if (e != cudaErrorInvalidConfiguration) return e;
     P.whole = 0;                            // the plan's buffers do not fit: split on the device
     P.cap = cap0;
   }
+  if (k_new) return cudaErrorNotSupported;
   return pick(P);
 }
 
@@ -1110,6 +1179,8 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   P.out = out;
   P.qk_scale = kLog2e / sqrtf((float)kD);
   P.whole = 0;
+  P.fuse = 0;
+  P.k_new = P.v_new = nullptr;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
   P.ns = 0;
   if (plan_whole(P, bounds, grid, wide_cap(cap0))) {

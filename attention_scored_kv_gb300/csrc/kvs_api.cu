@@ -22,6 +22,7 @@ bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                              int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
+                             const void* k_new, const void* v_new,
                              cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
 size_t static_scratch_limit();
@@ -411,10 +412,53 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (ctx->kernel == KVS_KERNEL_TENSOR) {
     return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
-                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, cs),
+                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, nullptr, nullptr, cs),
                    "tensor-core attend");
   }
   return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
+}
+
+kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_k,
+                             const void* d_v, const void* d_q, float* d_out, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (!d_k || !d_v) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL K or V");
+  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  if (ctx->kernel == KVS_KERNEL_TENSOR && ctx->plan.mode != KVS_MODE_H2O) {
+    const int B = ctx->cfg.max_seqs;
+    ctx->bounds.resize((size_t)n_seqs);
+    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+      const int64_t nx = ctx->next[(size_t)layer * B + s];
+      if (nx + 1 > ctx->cfg.max_positions)
+        return fail(ctx, KVS_ERR_CAPACITY, "sequence %d: position %lld + 1 exceeds max_positions %d", s,
+                    (long long)nx, ctx->cfg.max_positions);
+      ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
+    }
+    const cudaError_t e = launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
+                                           seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, d_k, d_v,
+                                           reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaErrorNotSupported) {
+      st = cuda_ok(ctx, e, "tensor-core append + attend");
+      if (st != KVS_OK) return st;
+      for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {   // the same shadow update as an append
+        int64_t& nx = ctx->next[(size_t)layer * B + s];
+        nx += 1;
+        if (nx > ctx->frontier[s]) {
+          ctx->h2o_bound[s] += cdiv64(nx, kBlock) - cdiv64(ctx->frontier[s], kBlock);
+          ctx->frontier[s] = nx;
+        }
+      }
+      return KVS_OK;
+    }
+  }
+  // no single-launch form for this context or launch: the two steps, same results
+  st = kvs_append_kv(ctx, layer, seq_begin, n_seqs, 1, d_k, d_v, stream);
+  if (st != KVS_OK) return st;
+  return kvs_decode_attend(ctx, layer, seq_begin, n_seqs, d_q, d_out, stream);
 }
 
 kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,

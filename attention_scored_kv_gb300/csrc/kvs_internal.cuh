@@ -100,9 +100,10 @@ struct SeqBlocks {
   int32_t k0, n;      // first block id and block count (H2O: k0 unused)
 };
 
-__device__ __forceinline__ SeqBlocks seq_blocks(const Dev& d, int layer, int s) {
+// The same for a given next position (NONE / WINDOW; H2O reads its resident count).
+__device__ __forceinline__ SeqBlocks seq_blocks_at(const Dev& d, int s, int64_t next) {
   SeqBlocks r;
-  r.next = d.next_pos[(size_t)layer * d.max_seqs + s];
+  r.next = next;
   r.lo = 0;
   if (d.mode == KVS_MODE_WINDOW && r.next > d.window) r.lo = r.next - d.window;
   if (r.next <= 0) { r.k0 = 0; r.n = 0; return r; }
@@ -110,6 +111,10 @@ __device__ __forceinline__ SeqBlocks seq_blocks(const Dev& d, int layer, int s) 
   r.k0 = (int32_t)(r.lo / kBlock);
   r.n = (int32_t)((r.next - 1) / kBlock) - r.k0 + 1;
   return r;
+}
+
+__device__ __forceinline__ SeqBlocks seq_blocks(const Dev& d, int layer, int s) {
+  return seq_blocks_at(d, s, d.next_pos[(size_t)layer * d.max_seqs + s]);
 }
 
 // Block id and page of the i-th resident block of sequence s.

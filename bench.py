@@ -258,6 +258,11 @@ def run_ours(args, world, rank, local):
         res_blocks = (wl.window // 16 + 1) if wl.window else lay.max_blocks
         k_sel, flags = wl0.keep_k(res_blocks), 0
     launches = {"n": 0}
+    # append + attend is one launch per layer with the tensor-core attend outside H2O mode
+    # when every sequence can have CTAs of its own; otherwise append and attend are two,
+    # and H2O adds one page allocation per step (the first layer to reach a new position)
+    fused = lay.attend_kernel == kvs.KERNEL_TENSOR and not wl.h2o_budget_tokens and B <= lay.attend_grid
+    per_step_launches = (L if fused else 2 * L) + 2 + (1 if wl.h2o_budget_tokens else 0)
 
     def step(t, q=None, k=None, v=None, out=None):
         q = Q[t] if q is None else q
@@ -265,11 +270,10 @@ def run_ours(args, world, rank, local):
         v = V[t] if v is None else v
         out = OUT if out is None else out
         for l in range(L):
-            cache.append_kv(l, k[l], v[l])
-            cache.decode_attend(l, q[l], out=out[l])
+            cache.append_attend(l, k[l], v[l], q[l], out=out[l])   # append + attend of one layer
         cache.accumulate_scores()
         cache.select_blocks(k_sel, flags=flags, keep_ids=keep_ids, keep_count=keep_cnt)
-        launches["n"] += 2 * L + 2 + (1 if wl.h2o_budget_tokens else 0)
+        launches["n"] += per_step_launches
 
     for t in range(eager):
         step(t % NI)
@@ -282,7 +286,6 @@ def run_ours(args, world, rank, local):
         with torch.cuda.graph(g):
             step(t)
         graphs.append(g)
-    per_step_launches = 2 * L + 2 + (1 if wl.h2o_budget_tokens else 0)
 
     for i in range(args.warmup):
         graphs[(eager + i) % NI].replay()

@@ -165,6 +165,22 @@ KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
 KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
                              const void* d_q, float* d_out, kvs_stream_t stream);
 
+/* One decode step of one layer in one call: kvs_append_kv of one new token per
+ * sequence (d_k, d_v: [n_seqs][1][num_kv_heads][head_dim] in in_dtype), then
+ * kvs_decode_attend (d_q, d_out as there).  No page counterpart as a single step: the
+ * pages append the decode token and attend over the cache including it, and this call
+ * does both.  With the tensor-core attend in NONE or WINDOW mode, and when every
+ * sequence of the range can have CTAs of its own, it is one kernel launch.  The CTA
+ * holding a sequence's newest block stores the token (the same bytes the append
+ * kernel stores) while the others stream, and the sequence's next_position advances
+ * when its last CTA leaves.  Otherwise it issues the two calls.  Same results, state
+ * and errors as the two calls.  If the launch reports KVS_ERR_TIMEOUT, the token may
+ * be stored without next_position having advanced: append it again after
+ * kvs_clear_error. */
+KVS_API kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                             const void* d_k, const void* d_v, const void* d_q, float* d_out,
+                             kvs_stream_t stream);
+
 /* kvs_decode_attend without any exchange area from the caller.  No page counterpart:
  * this is a deployment variant, not a step of the method.
  *

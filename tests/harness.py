@@ -100,8 +100,9 @@ class StateView:
 class Run:
     """One workload on the GPU, with the oracle tracking ``oracle_seqs``."""
 
-    def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0):
+    def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0, fused=False):
         self.wl = wl
+        self.fused = fused            # decode steps through append_attend (one call per layer)
         self.inp = workloads.Inputs(wl, device=device)
         self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit))
         self.oseqs = list(oracle_seqs)
@@ -148,9 +149,12 @@ class Run:
         res = {"out_err": 0.0}
         for l in range(wl.num_layers):
             k, v = self.inp.step_kv(l, t)
-            c.append_kv(l, k, v)
             q = self.inp.step_q(l, t)
-            out = c.decode_attend(l, q)
+            if self.fused:
+                out = c.append_attend(l, k, v, q)
+            else:
+                c.append_kv(l, k, v)
+                out = c.decode_attend(l, q)
             self.last_out[l] = out
             if self.oracle is not None:
                 kf, vf, qf = workloads.as_f64(k), workloads.as_f64(v), workloads.as_f64(q)

@@ -7,6 +7,8 @@ E4M3 codes, scales, slots and absolute positions bit-exact; attention output wit
 masses and score tables within 1e-4 absolute; kept block sets equal except for
 blocks whose oracle score lies within 1e-4 of the cut-off.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -18,8 +20,8 @@ from tests import harness
 pytestmark = pytest.mark.gpu
 
 
-def _full_check(wl, kernel=kvs.KERNEL_AUTO, steps=None, every=1):
-    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kernel)
+def _full_check(wl, kernel=kvs.KERNEL_AUTO, steps=None, every=1, fused=False):
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kernel, fused=fused)
     run.prefill()
     worst = 0.0
     n = wl.steps if steps is None else steps
@@ -70,6 +72,52 @@ def test_tensor_kernel_small(name):
     wl = SMALL[name]
     run, worst = _full_check(wl, kernel=kvs.KERNEL_TENSOR, every=3)
     assert run.cache.layout().attend_kernel == kvs.KERNEL_TENSOR
+
+
+@pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-nowindow", "e4m3-b16-window", "e4m3-h2o"])
+def test_fused_append_attend_against_oracle(name):
+    """append_attend (one launch per layer where the context allows; two calls for H2O)
+    against the oracle, every step."""
+    _full_check(SMALL[name], kernel=kvs.KERNEL_TENSOR, every=3, fused=True)
+
+
+def _state(cache, L):
+    names = [kvs.STATE_K_PAGES, kvs.STATE_V_PAGES, kvs.STATE_POSITIONS, kvs.STATE_TOKEN_MASS, kvs.STATE_BLOCK_MASS,
+             kvs.STATE_NEXT_POSITION]
+    if cache.cfg.kv_dtype == kvs.E4M3:
+        names += [kvs.STATE_K_SCALES, kvs.STATE_V_SCALES]
+    return {(n, l): cache.read_state(n, l).cpu() for n in names for l in range(L)}
+
+
+@pytest.mark.parametrize("name,steps", [("e4m3-b16-window", 20), ("bf16", 18), ("e4m3-nowindow", 17)])
+def test_fused_append_attend_is_bitwise_the_two_calls(name, steps):
+    """The single-launch form stores the same bytes and computes the same outputs and
+    masses, bit for bit, as append_kv followed by decode_attend (the window wraps and
+    blocks fill and start during these steps)."""
+    wl = dataclasses.replace(SMALL[name], steps=steps)
+    a = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR)
+    b = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR, fused=True)
+    a.prefill()
+    b.prefill()
+    for t in range(steps):
+        a.decode_step(select=False)
+        b.decode_step(select=False)
+        for l in range(wl.num_layers):
+            assert torch.equal(a.last_out[l], b.last_out[l]), (t, l)
+    sa, sb = _state(a.cache, wl.num_layers), _state(b.cache, wl.num_layers)
+    for key in sa:
+        assert torch.equal(sa[key], sb[key]), key
+    for n in (kvs.STATE_C_TOKEN, kvs.STATE_E_TOKEN, kvs.STATE_C_BLOCK, kvs.STATE_E_BLOCK):
+        assert torch.equal(a.cache.read_state(n).cpu(), b.cache.read_state(n).cpu()), n
+    assert a.cache.get_status() == 0 and b.cache.get_status() == 0
+
+
+def test_fused_append_attend_from_an_empty_cache():
+    """The first token of every sequence through append_attend (no entry before it), then
+    a few more: one block per sequence, fewer blocks than CTAs."""
+    wl = workloads.scaled_down("e4m3-b16-ctx32768-window4096", name="fused-empty", num_layers=2, batch=4,
+                               context=0, window=64, steps=20, prefill_chunk=0)
+    _full_check(wl, kernel=kvs.KERNEL_TENSOR, every=1, fused=True)
 
 
 @pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-h2o"])
