@@ -192,6 +192,27 @@ class KVCache:
                                             cap, _ptr(keep_count), _stream(stream)))
         return keep_ids, keep_count
 
+    def accumulate_select(self, k, seq_begin=0, n_seqs=None, score_kind=SCORE_CUMULATIVE, flags=0,
+                          keep_capacity=None, keep_ids=None, keep_count=None, stream=None):
+        """accumulate_scores then select_blocks (same arguments and results as the
+        latter), in one launch for sequences of at most 512 resident blocks."""
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        cap = self.layout().max_blocks if keep_capacity is None else keep_capacity
+        if keep_ids is None:
+            keep_ids = torch.full((n, cap), -1, dtype=torch.int32, device=self.device)
+        if keep_count is None:
+            keep_count = torch.zeros(n, dtype=torch.int32, device=self.device)
+        _need(keep_ids, "keep_ids", torch.int32, (n, cap))
+        _need(keep_count, "keep_count", torch.int32, (n,))
+        if isinstance(k, torch.Tensor):
+            _need(k, "k", torch.int32, (n,))
+            kp, ku = _ptr(k), 0
+        else:
+            kp, ku = None, int(k)
+        self._check(lib().kvs_accumulate_select(self._ctx, seq_begin, n, kp, ku, score_kind, flags, _ptr(keep_ids),
+                                                cap, _ptr(keep_count), _stream(stream)))
+        return keep_ids, keep_count
+
     # ---- inspection
     def read_state(self, what, layer=0, stream=None):
         """A raw copy (uint8 CUDA tensor) of one state array; see kvs_state_item."""

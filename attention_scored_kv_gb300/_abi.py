@@ -60,6 +60,7 @@ _SIGS = {
     "kvs_decode_attend_static_scratch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "kvs_accumulate_scores": (_I, [_P, _I, _I, _P]),
     "kvs_select_blocks": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
+    "kvs_accumulate_select": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
     "kvs_state_bytes": (ctypes.c_size_t, [_P, _I]),
     "kvs_read_state": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
     "kvs_get_layout": (_I, [_P, ctypes.POINTER(Layout)]),

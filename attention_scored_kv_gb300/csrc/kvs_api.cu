@@ -536,6 +536,48 @@ kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, co
   return KVS_OK;
 }
 
+kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const int32_t* d_k_per_seq,
+                                 int32_t k_uniform, int32_t score_kind, uint32_t flags, int32_t* d_keep_ids,
+                                 int32_t keep_capacity, int32_t* d_keep_count, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (score_kind != KVS_SCORE_CUMULATIVE && score_kind != KVS_SCORE_EMA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE or EMA");
+  if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
+  if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
+  if (!d_k_per_seq && k_uniform < 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "k must be >= 0");
+  if (!d_keep_ids || !d_keep_count || keep_capacity < 1)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "keep buffers missing or keep_capacity < 1");
+  const int B = ctx->cfg.max_seqs;
+  int64_t maxb = 1;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    const int64_t n0 = ctx->next[s];
+    for (int l = 1; l < ctx->cfg.num_layers; ++l)
+      if (ctx->next[(size_t)l * B + s] != n0)
+        return fail(ctx, KVS_ERR_STATE, "sequence %d: layers disagree on next_position", s);
+    maxb = std::max(maxb, seq_block_bound(ctx, s));
+  }
+  if (maxb > accumulate_select_max_blocks()) {   // long sequences: the two kernels
+    st = kvs_accumulate_scores(ctx, seq_begin, n_seqs, stream);
+    if (st != KVS_OK) return st;
+    return kvs_select_blocks(ctx, seq_begin, n_seqs, d_k_per_seq, k_uniform, score_kind, flags, d_keep_ids,
+                             keep_capacity, d_keep_count, stream);
+  }
+  st = cuda_ok(ctx, launch_accumulate_select(ctx->dev, seq_begin, n_seqs, (int)maxb, d_k_per_seq, k_uniform, score_kind, flags,
+                                             d_keep_ids, keep_capacity, d_keep_count,
+                                             reinterpret_cast<cudaStream_t>(stream)),
+               "accumulate + select");
+  if (st != KVS_OK) return st;
+  if ((flags & KVS_SELECT_APPLY) && !d_k_per_seq) {   // as kvs_select_blocks
+    const int64_t prot = cdiv64(ctx->cfg.h2o_sink_tokens, kBlock) + cdiv64(ctx->plan.recent_tokens, kBlock) + 1;
+    const int64_t kept = std::max<int64_t>(k_uniform, (flags & KVS_SELECT_PROTECT) ? prot : 0);
+    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) ctx->h2o_bound[s] = std::min(ctx->h2o_bound[s], kept);
+  }
+  return KVS_OK;
+}
+
 size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
   if (!ctx) return 0;
   const size_t slots = (size_t)ctx->plan.num_pages * kBlock, B = ctx->cfg.max_seqs, MB = ctx->plan.max_blocks;

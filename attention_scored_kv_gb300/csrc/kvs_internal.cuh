@@ -167,6 +167,10 @@ cudaError_t launch_append(const Dev& d, int layer, int seq_begin, int n_seqs, in
                           const void* k, const void* v, cudaStream_t st);
 cudaError_t launch_attend_general(const Dev& d, int layer, int seq_begin, int n_seqs,
                                   const void* q, float* out, cudaStream_t st);
+int accumulate_select_max_blocks();
+cudaError_t launch_accumulate_select(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+                                     const int32_t* k_per_seq, int k_uniform, int score_kind, uint32_t flags,
+                                     int32_t* keep_ids, int keep_capacity, int32_t* keep_count, cudaStream_t st);
 cudaError_t launch_accumulate(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
                               cudaStream_t st);
 cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,

@@ -1,0 +1,62 @@
+// One step's update of the score tables for one entry and one block: shared by the
+// accumulate kernel and the fused accumulate + select kernel, so both write identical
+// values.
+//
+// "Context views at marginal cost", Tier 1: running reductions, O(1) per entry per
+// step.  Flash-MoE "Context Optimization", H2O > How It Works, step 1: the token score
+// sums the post-softmax weights over all heads (and, here, all layers) and all steps.
+// "Per-Head Attention as a Scoring Signal": the block score is the maximum over heads
+// (and layers).  Token score x_p = sum_l tau_l[p] (float64 sum of the float32 layer
+// masses, layers in order); block score y_k = max_l beta_l[k]; C += x;
+// E <- d*E + (1-d)*x.  The decay of entries not updated for a while is applied lazily:
+// each entry keeps the step at which E was last written and a reader multiplies by
+// d^(steps elapsed).
+#pragma once
+#include "kvs_internal.cuh"
+
+namespace kvs {
+
+// EMA value as of step `step - 1` of an entry last written at step `last` (-1: never).
+// An entry resident in the previous step (the common case) needs no power at all.
+__device__ __forceinline__ double decayed(double e, int32_t last, int32_t step, double dec) {
+  if (last < 0) return 0.0;
+  const int32_t gap = step - 1 - last;
+  if (gap == 0) return e;
+  if (gap == 1) return e * dec;
+  return e * pow(dec, (double)gap);
+}
+
+// Entry p of sequence s, stored in (page, slot), at step `step`.
+__device__ __forceinline__ void update_entry(const Dev& d, int s, int64_t p, int32_t page, int32_t slot,
+                                             int32_t step) {
+  double x = 0.0;
+  for (int l = 0; l < d.L; ++l)
+    x += (double)d.tok_mass[(size_t)l * d.slot_layer_elems + (size_t)page * kBlock + slot];
+  const size_t t = (size_t)s * d.max_positions + p;
+  const int32_t last = d.last_tok[t];
+  const double e_prev = decayed(d.e_tok[t], last, step, d.ema_decay);
+  d.c_tok[t] += x;
+  d.e_tok[t] = d.ema_decay * e_prev + (1.0 - d.ema_decay) * x;
+  d.last_tok[t] = step;
+}
+
+// Block k of sequence s at step `step`; returns the new cumulative score in *c_new and
+// the new EMA in *e_new.
+__device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int32_t step, double* c_new,
+                                             double* e_new) {
+  float y = 0.f;
+  for (int l = 0; l < d.L; ++l)
+    y = fmaxf(y, d.blk_mass[(size_t)l * d.blk_layer_elems + (size_t)s * d.max_blocks + k]);
+  const size_t t = (size_t)s * d.max_blocks + k;
+  const int32_t last = d.last_blk[t];
+  const double e_prev = decayed(d.e_blk[t], last, step, d.ema_decay);
+  const double c = d.c_blk[t] + (double)y;
+  const double e = d.ema_decay * e_prev + (1.0 - d.ema_decay) * (double)y;
+  d.c_blk[t] = c;
+  d.e_blk[t] = e;
+  d.last_blk[t] = step;
+  *c_new = c;
+  *e_new = e;
+}
+
+}  // namespace kvs

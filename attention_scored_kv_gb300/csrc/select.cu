@@ -13,7 +13,7 @@
 // over the key bytes (histogram in shared memory, bucket found by one warp scan) finds
 // the key T of the k-th best and how many candidates equal to T to take; a stable
 // compaction in id order then emits every key > T and the first ties in id order.
-#include "kvs_internal.cuh"
+#include "select_key.cuh"
 
 namespace kvs {
 
@@ -22,10 +22,6 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kSmemCap = 6144;          // candidates whose keys stay in shared memory
 
-__device__ __forceinline__ uint64_t order_key(double v) {
-  const uint64_t b = (uint64_t)__double_as_longlong(v);
-  return (b >> 63) ? ~b : (b | 0x8000000000000000ull);
-}
 
 struct SelShared {
   uint32_t hist[256];
@@ -35,27 +31,6 @@ struct SelShared {
   int32_t n_prot;
 };
 
-__device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlocks& sb, int i, int kind,
-                                             bool protect, int32_t* kid, int32_t* page) {
-  const int32_t k = block_at(d, s, sb, i, page);
-  *kid = k;
-  if (protect) {
-    const int64_t b0 = (int64_t)k * kBlock, b1 = b0 + kBlock;       // block holds [b0, b1)
-    const bool sink = b0 < d.h2o_sink_tokens;
-    const bool recent = b1 > sb.next - d.h2o_recent_tokens;
-    if (sink || recent) return ~0ull;
-  }
-  const size_t t = (size_t)s * d.max_blocks + k;
-  double v;
-  if (kind == KVS_SCORE_CUMULATIVE) {
-    v = d.c_blk[t];
-  } else {
-    const int32_t last = d.last_blk[t];
-    const int32_t gap = d.steps[s] - 1 - last;
-    v = (last < 0) ? 0.0 : (gap == 0 ? d.e_blk[t] : d.e_blk[t] * pow(d.ema_decay, (double)gap));
-  }
-  return order_key(v);
-}
 
 // Block-wide exclusive scan of one flag per thread; returns the exclusive prefix and
 // writes the total to *total.  All threads must call it.
@@ -100,7 +75,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
   int cnt = 0;
   for (int i = tid; i < n; i += kThreads) {
     int32_t k, page;
-    const uint64_t key = cand_key(d, s, sb, i, kind, protect, &k, &page);
+    const uint64_t key = cand_key<false>(d, s, sb, i, kind, protect, d.steps[s], &k, &page);
     cnt += key == ~0ull;
     if (in_smem) { skey[i] = key; sid[i] = k; spage[i] = page; }
   }
@@ -111,7 +86,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
 
   auto key_of = [&](int i, int32_t* k, int32_t* page) -> uint64_t {
     if (in_smem) { *k = sid[i]; *page = spage[i]; return skey[i]; }
-    return cand_key(d, s, sb, i, kind, protect, k, page);
+    return cand_key<false>(d, s, sb, i, kind, protect, d.steps[s], k, page);
   };
 
   // radix select of the kk-th largest key (k = 0 keeps nothing: T above every key)

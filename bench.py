@@ -260,9 +260,13 @@ def run_ours(args, world, rank, local):
     launches = {"n": 0}
     # append + attend is one launch per layer with the tensor-core attend outside H2O mode
     # when every sequence can have CTAs of its own; otherwise append and attend are two,
-    # and H2O adds one page allocation per step (the first layer to reach a new position)
+    # and H2O adds one page allocation per step (the first layer to reach a new position).
+    # accumulate + select is one launch up to 512 resident blocks per sequence.
     fused = lay.attend_kernel == kvs.KERNEL_TENSOR and not wl.h2o_budget_tokens and B <= lay.attend_grid
-    per_step_launches = (L if fused else 2 * L) + 2 + (1 if wl.h2o_budget_tokens else 0)
+    res_bound = (wl.window // 16 + 1) if wl.window else (
+        wl.h2o_budget_tokens // 16 + 2 if wl.h2o_budget_tokens else lay.max_blocks)
+    per_step_launches = ((L if fused else 2 * L) + (1 if res_bound <= 512 else 2)
+                         + (1 if wl.h2o_budget_tokens else 0))
 
     def step(t, q=None, k=None, v=None, out=None):
         q = Q[t] if q is None else q
@@ -271,8 +275,7 @@ def run_ours(args, world, rank, local):
         out = OUT if out is None else out
         for l in range(L):
             cache.append_attend(l, k[l], v[l], q[l], out=out[l])   # append + attend of one layer
-        cache.accumulate_scores()
-        cache.select_blocks(k_sel, flags=flags, keep_ids=keep_ids, keep_count=keep_cnt)
+        cache.accumulate_select(k_sel, flags=flags, keep_ids=keep_ids, keep_count=keep_cnt)
         launches["n"] += per_step_launches
 
     for t in range(eager):

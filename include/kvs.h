@@ -241,6 +241,20 @@ KVS_API kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_
                              uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                              int32_t* d_keep_count, kvs_stream_t stream);
 
+/* kvs_accumulate_scores followed by kvs_select_blocks (same arguments as the latter),
+ * in one launch when every sequence of the range has at most 512 resident blocks.
+ * There is no page counterpart as a single step: the pages fold a step's weights into
+ * the scores and then pick the blocks to keep, and this call does both.  The tables
+ * are updated exactly as the accumulate kernel does, on its grid.  The last CTA of
+ * each sequence to finish ranks the blocks just scored: rank = keys above + equal keys
+ * with a lower id, which keeps the same set as the radix select.  It then compacts the
+ * kept ids in id order.  Longer sequences: the two calls.  Same results, state and
+ * errors as the two calls. */
+KVS_API kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
+                                 const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
+                                 uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
+                                 int32_t* d_keep_count, kvs_stream_t stream);
+
 /* State read-back (tests, inspection).  Copies one array of `layer` (ignored for
  * per-sequence items) into d_dst (device), which must hold kvs_state_bytes(). */
 typedef enum {

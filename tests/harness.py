@@ -143,7 +143,7 @@ class Run:
             self.oracle.append(l, i, kf[a:a + chunk], vf[a:a + chunk])
 
     # ------------------------------------------------------------------ one decode step
-    def decode_step(self, select=True, compare_outputs=True):
+    def decode_step(self, select=True, compare_outputs=True, accumulate=True):
         """Run one step on both sides; returns a dict of oracle-vs-GPU results."""
         wl, c, t = self.wl, self.cache, self.step
         res = {"out_err": 0.0}
@@ -164,9 +164,10 @@ class Run:
                     if compare_outputs:
                         got = out[s].double().cpu().numpy()
                         res["out_err"] = max(res["out_err"], rel_err_rows(got, ref))
-        c.accumulate_scores()
-        if self.oracle is not None:
-            res["oracle_step"] = self.oracle.accumulate()
+        if accumulate:
+            c.accumulate_scores()
+            if self.oracle is not None:
+                res["oracle_step"] = self.oracle.accumulate()
         if select:
             res["keep"] = self.select()
         self.step += 1

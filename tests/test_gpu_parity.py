@@ -120,6 +120,58 @@ def test_fused_append_attend_from_an_empty_cache():
     _full_check(wl, kernel=kvs.KERNEL_TENSOR, every=1, fused=True)
 
 
+@pytest.mark.parametrize("name,kind,krule", [
+    ("e4m3-b16-window", kvs.SCORE_CUMULATIVE, "per-seq"),
+    ("bf16", kvs.SCORE_EMA, 3),
+    ("e4m3-nowindow", kvs.SCORE_EMA, 0),
+    ("e4m3-window", kvs.SCORE_CUMULATIVE, 10 ** 6),
+    ("e4m3-h2o", kvs.SCORE_CUMULATIVE, "h2o"),
+    ("e4m3-h2o", kvs.SCORE_EMA, "h2o"),
+])
+def test_accumulate_select_is_bitwise_the_two_calls(name, kind, krule):
+    """accumulate_select (one launch) keeps the same ids and writes the same tables, bit
+    for bit, as accumulate_scores then select_blocks: per-sequence and uniform k, k = 0,
+    k above the block count, cumulative and EMA keys, H2O protection with eviction."""
+    wl = dataclasses.replace(SMALL[name], steps=min(SMALL[name].steps, 12))
+    runs = [harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR) for _ in range(2)]
+    for r in runs:
+        r.prefill()
+    h2o = krule == "h2o"
+    for t in range(wl.steps):
+        outs = []
+        for j, r in enumerate(runs):
+            r.decode_step(select=False, accumulate=False)
+            c = r.cache
+            cap = c.layout().max_blocks
+            if h2o:
+                k, flags = wl.h2o_budget_tokens // 16, kvs.SELECT_PROTECT | kvs.SELECT_APPLY
+            elif krule == "per-seq":
+                k = torch.tensor([(3 * s + t) % 9 for s in range(wl.batch)], dtype=torch.int32, device="cuda")
+                flags = 0
+            else:
+                k, flags = krule, 0
+            if j == 0:
+                c.accumulate_scores()
+                ids, cnt = c.select_blocks(k, score_kind=kind, flags=flags, keep_capacity=cap)
+            else:
+                ids, cnt = c.accumulate_select(k, score_kind=kind, flags=flags, keep_capacity=cap)
+            outs.append((ids.cpu(), cnt.cpu()))
+        assert torch.equal(outs[0][1], outs[1][1]), t
+        for s in range(wl.batch):
+            n = int(outs[0][1][s])
+            assert torch.equal(outs[0][0][s, :n], outs[1][0][s, :n]), (t, s)
+    a, b = runs[0].cache, runs[1].cache
+    for n in (kvs.STATE_C_TOKEN, kvs.STATE_E_TOKEN, kvs.STATE_C_BLOCK, kvs.STATE_E_BLOCK, kvs.STATE_STEPS):
+        assert torch.equal(a.read_state(n).cpu(), b.read_state(n).cpu()), n
+    if h2o:
+        # the same blocks stay resident; which free page a block gets depends on the order
+        # in which evicted pages were pushed (atomics), in either form
+        bta = a.read_state(kvs.STATE_BLOCK_TABLE).cpu().view(torch.int32)
+        btb = b.read_state(kvs.STATE_BLOCK_TABLE).cpu().view(torch.int32)
+        assert torch.equal(bta >= 0, btb >= 0)
+    assert a.get_status() == 0 and b.get_status() == 0
+
+
 @pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-h2o"])
 def test_general_kernel_on_tensor_shapes(name):
     wl = SMALL[name]
