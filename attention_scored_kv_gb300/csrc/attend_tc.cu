@@ -428,6 +428,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
 
+  // everything below may read what the previous kernel of the stream wrote; let the next
+  // kernel's launch begin now (it too waits for this one before reading anything)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
   // ---------------------------------------------------------------- partition
   int x0 = 0;                               // whole plan: block index within the sequence
   int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole plan)
@@ -958,11 +963,16 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  // cooperative: every CTA resident at once (the cross-CTA waits rely on it);
+  // programmatic serialisation: the launch may begin while the previous kernel of the
+  // stream finishes; the kernel waits for it (griddepcontrol.wait) before reading state
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, fn, tk, tv, d, P);
 }
 
