@@ -153,11 +153,16 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3) : "r"(addr));
 }
 
-// Logit / weight store: per local block i, [HQ][16] floats; the 4-float chunk index of
-// a position is XOR-ed with bits of the head so both access patterns spread over banks.
+// Logit / weight store: per local block i, [HQ][16] floats then 16 floats of padding
+// (kLgPad: consecutive blocks start 64 bytes apart modulo 128, so reads of two blocks
+// in one quarter-warp fall in different banks); the 4-float chunk index of a position
+// is XOR-ed with bits of the head so both access patterns spread over banks.
+constexpr int kLgPad = 16;
+template <int HQ>
+__host__ __device__ constexpr int lg_block() { return HQ * kBlock + kLgPad; }
 template <int HQ>
 __device__ __forceinline__ int lidx(int i, int h, int pos) {
-  return (i * HQ + h) * kBlock + ((((pos >> 2) ^ (h >> 1)) & 3) << 2) + (pos & 3);
+  return i * lg_block<HQ>() + h * kBlock + ((((pos >> 2) ^ (h >> 1)) & 3) << 2) + (pos & 3);
 }
 
 // CTA holding global block x when CTA c holds q + (c < r) blocks.
@@ -269,7 +274,7 @@ __device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* ssc
     *pb = make_float2(p[b][2], p[b][3]);
     bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
     bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-    if (t == 0) bsum[i * HQ + hg] = bpart;
+    if (t == 0) bsum[i * (HQ + 1) + hg] = bpart;        // rows padded by one float
   }
   if constexpr (FP8) {
     uint32_t b0[NB], b1[NB];
@@ -378,9 +383,9 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   p.flag = o;   o += 16;
   p.pm = o;     o += (size_t)kSC * HQ * 4;
   p.pl = o;     o += (size_t)kSC * HQ * 4;
-  p.bsum = o;   o = up16(o + (size_t)cap * HQ * 4);
+  p.bsum = o;   o = up16(o + (size_t)cap * (HQ + 1) * 4);
   p.obuf = o;   o += (WPK == 2 ? (size_t)hkv * 32 * 32 * 4 : 0);
-  p.lg = o;     o += lsmem ? (size_t)cap * HQ * kBlock * 4 : 0;
+  p.lg = o;     o += lsmem ? (size_t)cap * (HQ * kBlock + kLgPad) * 4 : 0;
   p.total = o + 1024;                       // alignment slack
   return p;
 }
@@ -543,7 +548,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     return;
   }
 
-  float* lgbase = LSMEM ? lg_smem : d.logit_scratch + (size_t)c * P.cap * HQ * kBlock;
+  float* lgbase = LSMEM ? lg_smem : d.logit_scratch + (size_t)c * P.cap * lg_block<HQ>();
   const size_t lay_slot = (size_t)P.layer * d.slot_layer_elems;
   float* partials = d.partials;
 
@@ -835,26 +840,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       if (warp < kNCW / 2) {
         // masses: lane = (block bi = lane >> 2 of 8 per warp round, position chunk
         // c4 = lane & 3); each lane walks all heads for its 4 positions (no shuffles),
-        // block bi starting at head bi so that the 16-byte reads of one quarter-warp
-        // cover all banks
+        // the head factors read 8 at a time; the padded block strides keep the 16-byte
+        // weight reads and the bsum reads free of bank conflicts
         const int bi = lane >> 2, c4 = lane & 3;
         for (int ib = i0 + warp * 8; ib < i1; ib += (kNCW / 2) * 8) {
           const int i = ib + bi;
           if (i < i1) {
-            const float* lgi = lgbase + (size_t)i * HQ * kBlock;
-            const float* bsi = bsum + i * HQ;
+            const float* lgi = lgbase + (size_t)i * lg_block<HQ>();
+            const float* bsi = bsum + i * (HQ + 1);
             float4 tau = make_float4(0.f, 0.f, 0.f, 0.f);   // entry: sum over heads
             float bm = 0.f;                                 // block: max over heads
-#pragma unroll 8
-            for (int u = 0; u < HQ; ++u) {
-              const int h = (u + bi) & (HQ - 1);
-              const float f = cfac[h];
-              const float4 v = *reinterpret_cast<const float4*>(lgi + h * kBlock + (((c4 ^ (h >> 1)) & 3) << 2));
-              tau.x += v.x * f;
-              tau.y += v.y * f;
-              tau.z += v.z * f;
-              tau.w += v.w * f;
-              bm = fmaxf(bm, bsi[h] * f);
+#pragma unroll
+            for (int u0 = 0; u0 < HQ; u0 += 8) {
+              const float4 fa = *reinterpret_cast<const float4*>(cfac + u0);
+              const float4 fb = *reinterpret_cast<const float4*>(cfac + u0 + 4);
+              const float f[8] = {fa.x, fa.y, fa.z, fa.w, fb.x, fb.y, fb.z, fb.w};
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int h = u0 + u;
+                const float4 v = *reinterpret_cast<const float4*>(lgi + h * kBlock + (((c4 ^ (h >> 1)) & 3) << 2));
+                tau.x += v.x * f[u];
+                tau.y += v.y * f[u];
+                tau.z += v.z * f[u];
+                tau.w += v.w * f[u];
+                bm = fmaxf(bm, bsi[h] * f[u]);
+              }
             }
             const int64_t p0 = (int64_t)blk_id[i] * kBlock + 4 * c4;   // slots p % 16
             float* dst = d.tok_mass + lay_slot + (size_t)blk_page[i] * kBlock + 4 * c4;
@@ -1019,7 +1029,7 @@ cudaError_t launch_pick(const CUtensorMap& tk, const CUtensorMap& tv, const Dev&
   if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
   P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs);
   if (P.ns == 0) return cudaErrorInvalidConfiguration;
-  if ((size_t)grid * P.cap * Cfg<HKV, FP8>::HQ * kBlock > d.logit_scratch_elems) return cudaErrorInvalidConfiguration;
+  if ((size_t)grid * P.cap * lg_block<Cfg<HKV, FP8>::HQ>() > d.logit_scratch_elems) return cudaErrorInvalidConfiguration;
   return launch_one<HKV, FP8, false>(tk, tv, d, P, grid, st);
 }
 

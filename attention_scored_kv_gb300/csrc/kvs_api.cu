@@ -128,7 +128,7 @@ void make_plan(const kvs_config* c, Plan* p) {
   // logits: the general kernel needs [seq][Hq][entries]; the tensor kernel per-CTA shares
   const size_t res_total = std::min<size_t>(B * p->res_blocks_per_seq, p->mode == KVS_MODE_H2O ? NP : SIZE_MAX);
   const size_t gen = B * Hq * (size_t)p->res_blocks_per_seq * kBlock;
-  const size_t tcs = (res_total + 2 * (size_t)kGridMax) * Hq * kBlock;
+  const size_t tcs = (res_total + 2 * (size_t)kGridMax) * (Hq * kBlock + 16);   // + the per-block padding
   p->logit_elems = std::max(gen, tcs);
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t r = o; o = align256(o + bytes); return r; };
