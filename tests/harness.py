@@ -197,6 +197,30 @@ class Run:
                     ora[s] = self.oracle.select(i, int(ks[s].item()))
         return gpu, ora
 
+    def accumulate_select(self):
+        """The bench's end of a step: accumulate_select on the GPU (one launch); the
+        oracle accumulates, then selects with the same rule as select()."""
+        wl, c = self.wl, self.cache
+        lay = c.layout()
+        if self.oracle is not None:
+            self.oracle.accumulate()
+        if wl.h2o_budget_tokens > 0:
+            ids, cnt = c.accumulate_select(wl.h2o_budget_tokens // 16, flags=kvs.SELECT_PROTECT | kvs.SELECT_APPLY)
+            ks = None
+        else:
+            ks = torch.tensor([wl.keep_k(int(n)) for n in self.candidate_counts()], dtype=torch.int32, device="cuda")
+            ids, cnt = c.accumulate_select(ks, keep_capacity=lay.max_blocks)
+        ids, cnt = ids.cpu().numpy(), cnt.cpu().numpy()
+        gpu = {s: list(ids[s, :cnt[s]]) for s in range(wl.batch)}
+        ora = {}
+        if self.oracle is not None:
+            for i, s in enumerate(self.oseqs):
+                if wl.h2o_budget_tokens > 0:
+                    ora[s] = self.oracle.select(i, wl.h2o_budget_tokens // 16, protect=True, apply=True)
+                else:
+                    ora[s] = self.oracle.select(i, int(ks[s].item()))
+        return gpu, ora
+
     def candidate_counts(self):
         """Resident blocks per sequence, from the host-side rule of the mode."""
         wl = self.wl
