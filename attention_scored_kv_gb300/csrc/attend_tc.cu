@@ -47,6 +47,9 @@ namespace {
 constexpr int kD = 128;
 constexpr int kG = 8;
 constexpr int kNCW = 8;                 // consumer warps
+// A ring stage: every stage completion costs a few hundred ns of barrier traffic, so
+// stages are large (48 KB: 6 E4M3 or 3 bf16 blocks of 4 KV heads); two or more stages.
+constexpr int kStageBytes = 48 * 1024;
 constexpr int kThreads = (kNCW + 1) * 32;
 constexpr int kMbarLimit = 1 << 22;     // polls of an mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
@@ -58,7 +61,7 @@ struct Cfg {
   static constexpr int WPK = kNCW / HKV;                   // consumer warps per KV head
   static constexpr int ESZ = FP8 ? 1 : 2;
   static constexpr int BLK = HKV * kBlock * kD * ESZ;       // one block of K or V, all heads
-  static constexpr int SB = 32768 / BLK;                    // blocks per ring stage (32 KB)
+  static constexpr int SB = kStageBytes / BLK >= 1 ? kStageBytes / BLK : 1;   // blocks per ring stage
   static constexpr int STAGE = SB * BLK;
   static constexpr int HALF = HKV * kBlock * 128;           // bf16: bytes of one 64-dim half
 };
@@ -335,8 +338,6 @@ __device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* ssc
 constexpr int kSC = 32;                 // partial records per round of the normaliser
 constexpr int kRingBytes = 128 * 1024;  // shared memory given to the TMA ring at most
 constexpr int kMinStages = 2;
-constexpr int kStageBytes = 32768;      // a ring stage: each completion costs ~0.3 us, so
-                                        // stages are 32 KB (several 16-token blocks)
 
 struct Params {
   int layer, seq_begin, n_seqs, cap;   // cap: blocks per CTA the buffers hold
@@ -709,7 +710,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 #pragma unroll
           for (int rr = 0; rr < 4; ++rr) obuf[(kvh * 32 + mb * 4 + rr) * 32 + lane] = o[mb][rr];
       }
-      named_sync(1, kNCW * 32);
+      if (WPK == 2) named_sync(2 + kvh, 64);       // the two warps of KV head kvh
       if (sub == 0) {
         if (WPK == 2) {
 #pragma unroll
@@ -748,16 +749,26 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
           for (int w = 1; w < WPK; ++w) l += lbuf[w * HQ + h];
           d.part_ml[(size_t)(c + b) * HQ + h] = ((unsigned long long)__float_as_uint(l) << 32) | __float_as_uint(mseg[h]);
         }
+        // Each writer warp releases its own rows and words and arrives (HKV arrivals per
+        // CTA), without a return value: no CTA barrier on the way.  One poller per CTA
+        // reads the counter (every thread polling the records themselves floods their
+        // few L2 lines).
+        if (d.spin_limit >= 0) {
+          __syncwarp();
+          if (lane == 0) {
+            __threadfence();
+            red_add(ctr_base + (size_t)s * kCounterInts, 1);
+          }
+        }
       }
-      named_sync(1, kNCW * 32);
-      // release: the CTA barrier orders every writer's rows and words before this fence.
-      // The arrival order is needed only when nobody waits (spin_limit < 0); otherwise the
-      // increment goes out without a return value.  One poller per CTA reads the counter
-      // (every thread polling the records themselves floods their few L2 lines).
-      if (tid == 0) {
-        __threadfence();
-        if (d.spin_limit < 0) ticket[i0] = atomicAdd(ctr_base + (size_t)s * kCounterInts, 1);
-        else red_add(ctr_base + (size_t)s * kCounterInts, 1);
+      if (d.spin_limit < 0) {
+        // nobody waits: one arrival per CTA, with its order, after a CTA barrier; only
+        // the last CTA to arrive goes on
+        named_sync(1, kNCW * 32);
+        if (tid == 0) {
+          __threadfence();
+          ticket[i0] = atomicAdd(ctr_base + (size_t)s * kCounterInts, 1);
+        }
       }
       i0 = i1;
     }
@@ -781,7 +792,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       if (tid == 0) {
         // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
         const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1
-                                         : wait_at_least(ctr_base + (size_t)s * kCounterInts, S, d.spin_limit);
+                                         : wait_at_least(ctr_base + (size_t)s * kCounterInts, S * HKV, d.spin_limit);
         flag[0] = ok ? 1 : 0;
         if (!ok) set_error(d, kErrTimeout);
       }
