@@ -23,6 +23,7 @@ What one decode step computes (per layer l and sequence b, then per step):
       O(1)-per-entry running reductions; "Context Optimization", H2O step 1).
   a5  select: top-k resident blocks by C (or E) with ties to the lower block id;
       with H2O the sink and recent blocks are protected and eviction may be applied.
+  re-attend (Tier 2): a later query attends over the entries of the kept blocks only.
 
 Where the pages leave a step open, the module docstrings of ``attention``,
 ``selection`` and ``e4m3`` state the reading taken.
@@ -177,6 +178,19 @@ class OracleKV:
         self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(w))
         self._blk_mass[(layer, seq)] = attention.block_step_mass(w, pos, self.block)
         self._attended.add((layer, seq))
+        return out, w, pos
+
+    def attend_blocks(self, layer, seq, q, block_ids):
+        """Tier-2 re-attend ("Context views at marginal cost", Tier 2 and Fact 3): a new
+        query attends over the cached K and V of a selected subset only, here the
+        resident entries of the listed blocks (the blocks a selection kept).  Softmax
+        over that subset; no mass is recorded.  Returns (out [Hq, D], weights [Hq, n],
+        positions [n])."""
+        pos = self.resident_positions(layer, seq)
+        keep = np.isin(pos // self.block, np.asarray(sorted(set(int(b) for b in block_ids)), np.int64))
+        pos = pos[keep]
+        k, v = self.stored_kv(layer, seq, pos)
+        out, w = attention.decode_attention(q, k, v)
         return out, w, pos
 
     def token_mass(self, layer, seq):
