@@ -154,6 +154,23 @@ class KVCache:
                                             _ptr(out), _stream(stream)))
         return out
 
+    def attend_blocks(self, layer, q, block_ids, block_count, out=None, seq_begin=0, stream=None):
+        """Re-attend q over the resident entries of the listed blocks only (for example
+        the keep_ids and keep_count of select_blocks).  block_ids: int32 CUDA tensor
+        [n_seqs, stride]; block_count: int32 CUDA tensor [n_seqs]."""
+        _, Hq, _, D = self.shape
+        n_seqs = int(q.shape[0])
+        _need(q, "q", self.in_dtype, (n_seqs, Hq, D))
+        stride = int(block_ids.shape[1])
+        _need(block_ids, "block_ids", torch.int32, (n_seqs, stride))
+        _need(block_count, "block_count", torch.int32, (n_seqs,))
+        if out is None:
+            out = torch.empty((n_seqs, Hq, D), dtype=torch.float32, device=q.device)
+        _need(out, "out", torch.float32, (n_seqs, Hq, D))
+        self._check(lib().kvs_attend_blocks(self._ctx, layer, seq_begin, n_seqs, _ptr(block_ids), stride,
+                                            _ptr(block_count), _ptr(q), _ptr(out), _stream(stream)))
+        return out
+
     def decode_attend_static_scratch(self, layer, q, out=None, seq_begin=0, stream=None):
         """decode_attend with the exchange area in the library's own fixed array instead
         of this cache's workspace (for callers that cannot supply device memory)."""

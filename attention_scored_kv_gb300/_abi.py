@@ -57,6 +57,7 @@ _SIGS = {
     "kvs_append_kv": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "kvs_decode_attend": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "kvs_append_attend": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
+    "kvs_attend_blocks": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "kvs_decode_attend_static_scratch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "kvs_accumulate_scores": (_I, [_P, _I, _I, _P]),
     "kvs_select_blocks": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),

@@ -356,7 +356,28 @@ struct Params {
   int fuse;
   const void* k_new;
   const void* v_new;
+  // Block list (list_ids non-null): attend over the resident entries of the listed
+  // blocks only, list_ids[b * list_stride + i] for i < list_count[b]; no masses.
+  const int32_t* list_ids;
+  const int32_t* list_count;
+  int list_stride;
 };
+
+// Page of block k of sequence s for a block list: the slot rule of the mode, or the
+// block table (H2O).  A block id out of range or not resident (H2O) is reported, and
+// the block then reads page 0 with every position masked (k = -1).
+__device__ __forceinline__ int32_t list_block(const Dev& d, int s, int32_t* k) {
+  int32_t page = -1, slot;
+  if (*k >= 0 && *k < d.max_blocks)
+    page = d.mode == KVS_MODE_H2O ? d.block_table[(size_t)s * d.max_blocks + *k]
+                                  : page_of(d, s, (int64_t)*k * kBlock, &slot);
+  if (page < 0 || page >= d.num_pages) {
+    set_error(d, kErrState);
+    *k = -1;
+    page = 0;
+  }
+  return page;
+}
 
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
 // so every stage keeps the 1024-byte alignment the 128-byte swizzle needs.
@@ -460,6 +481,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const bool grow = P.fuse && nxt < d.max_positions;
       if (P.fuse && !grow && tid == 0) set_error(d, kErrCapacity);
       sbw = seq_blocks_at(d, P.seq_begin + lo, grow ? nxt + 1 : nxt);
+      if (P.list_ids) sbw.n = min(max(P.list_count[lo], 0), P.list_stride);
       const int cb = P.cst[lo + 1] - P.cst[lo], rk = c - P.cst[lo];
       const int qb = sbw.n / cb, rb = sbw.n % cb;
       x0 = rk * qb + (rk < rb ? rk : rb);
@@ -475,7 +497,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const int b = b0 + lane;
         int nb = 0;
         if (b < P.n_seqs) {
-          const SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
+          SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
+          if (P.list_ids) sb.n = min(max(P.list_count[b], 0), P.list_stride);
           seqb[b] = sb;
           nb = sb.n;
         }
@@ -505,8 +528,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   }
   if (cseq >= 0) {
     for (int i = tid; i < nblk; i += kThreads) {
-      int32_t page;
-      blk_id[i] = block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+      int32_t page, k;
+      if (P.list_ids) {
+        k = P.list_ids[(size_t)cseq * P.list_stride + x0 + i];
+        page = list_block(d, P.seq_begin + cseq, &k);
+      } else {
+        k = block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+      }
+      blk_id[i] = k;
       blk_page[i] = page;
       blk_seq[i] = cseq;
     }
@@ -518,8 +547,14 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const int mid = (lo + hi + 1) >> 1;
         if (prefix[mid] <= x) lo = mid; else hi = mid - 1;
       }
-      int32_t page;
-      blk_id[i] = block_at(d, P.seq_begin + lo, seqb[lo], x - prefix[lo], &page);
+      int32_t page, k;
+      if (P.list_ids) {
+        k = P.list_ids[(size_t)lo * P.list_stride + x - prefix[lo]];
+        page = list_block(d, P.seq_begin + lo, &k);
+      } else {
+        k = block_at(d, P.seq_begin + lo, seqb[lo], x - prefix[lo], &page);
+      }
+      blk_id[i] = k;
       blk_page[i] = page;
       blk_seq[i] = lo;
     }
@@ -849,6 +884,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const bool fac_in_smem = S <= kSC;
 
       if (warp < kNCW / 2) {
+        if (!P.list_ids) {                         // (a block-list attend records no mass)
         // masses: lane = (block bi = lane >> 2 of 8 per warp round, position chunk
         // c4 = lane & 3); each lane walks all heads for its 4 positions (no shuffles),
         // the head factors read 8 at a time; the padded block strides keep the 16-byte
@@ -890,6 +926,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             if (c4 == 0)
               d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
           }
+        }
         }
       } else {
         // output: this CTA combines heads h with h % S == its rank among the sequence's
@@ -1079,12 +1116,15 @@ cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int
 // Blocks one CTA must hold for a launch whose resident blocks number at most T_bound.
 int tc_cap(int64_t T_bound, int grid) { return (int)((T_bound + grid - 1) / grid); }
 
-// k_new / v_new non-null: append one token per sequence in the same launch (NONE and
-// WINDOW modes, whole-CTA plan); cudaErrorNotSupported when that plan is not possible
-// or its buffers do not fit.
+// opt.k_new / v_new non-null: append one token per sequence in the same launch (NONE
+// and WINDOW modes, whole-CTA plan); cudaErrorNotSupported when that plan is not
+// possible or its buffers do not fit.  opt.list_ids non-null: attend over the listed
+// blocks only (bounds then bound the list lengths).
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                              int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
-                             int grid, const void* k_new, const void* v_new, cudaStream_t st) {
+                             int grid, const AttendOpts& opt, cudaStream_t st) {
+  const void* k_new = opt.k_new;
+  const void* v_new = opt.v_new;
   Params P;
   P.layer = layer;
   P.seq_begin = seq_begin;
@@ -1100,6 +1140,9 @@ cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const
   P.whole = 0;
   P.fuse = 0;
   P.k_new = P.v_new = nullptr;
+  P.list_ids = opt.list_ids;
+  P.list_count = opt.list_count;
+  P.list_stride = opt.list_stride;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
   auto pick = [&](const Params& PP) {
     if (d.Hkv == 4) return fp8 ? launch_pick<4, true>(tk, tv, d, PP, grid, st) : launch_pick<4, false>(tk, tv, d, PP, grid, st);
@@ -1212,6 +1255,8 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   P.whole = 0;
   P.fuse = 0;
   P.k_new = P.v_new = nullptr;
+  P.list_ids = P.list_count = nullptr;
+  P.list_stride = 0;
   const bool fp8 = d.kv_dtype == KVS_E4M3;
   P.ns = 0;
   if (plan_whole(P, bounds, grid, wide_cap(cap0))) {

@@ -22,8 +22,7 @@ bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                              int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
-                             const void* k_new, const void* v_new,
-                             cudaStream_t st);
+                             const AttendOpts& opt, cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
 size_t static_scratch_limit();
 size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* ml_offset);
@@ -412,7 +411,7 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (ctx->kernel == KVS_KERNEL_TENSOR) {
     return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
-                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, nullptr, nullptr, cs),
+                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, AttendOpts{}, cs),
                    "tensor-core attend");
   }
   return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
@@ -438,8 +437,11 @@ kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
                     (long long)nx, ctx->cfg.max_positions);
       ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
     }
+    AttendOpts opt;
+    opt.k_new = d_k;
+    opt.v_new = d_v;
     const cudaError_t e = launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
-                                           seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, d_k, d_v,
+                                           seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaErrorNotSupported) {
       st = cuda_ok(ctx, e, "tensor-core append + attend");
@@ -459,6 +461,37 @@ kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   st = kvs_append_kv(ctx, layer, seq_begin, n_seqs, 1, d_k, d_v, stream);
   if (st != KVS_OK) return st;
   return kvs_decode_attend(ctx, layer, seq_begin, n_seqs, d_q, d_out, stream);
+}
+
+kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                             const int32_t* d_block_ids, int32_t ids_stride, const int32_t* d_block_count,
+                             const void* d_q, float* d_out, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (!d_block_ids || !d_block_count || ids_stride < 1)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "block list missing or ids_stride < 1");
+  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  if (ctx->kernel != KVS_KERNEL_TENSOR)
+    return fail(ctx, KVS_ERR_UNSUPPORTED, "the block-list attend runs on the tensor-core attend only");
+  const int B = ctx->cfg.max_seqs;
+  ctx->bounds.resize((size_t)n_seqs);
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    if (ctx->next[(size_t)layer * B + s] == 0)
+      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
+    ctx->bounds[s - seq_begin] = (int32_t)std::min<int64_t>(ids_stride, seq_block_bound(ctx, s));
+  }
+  AttendOpts opt;
+  opt.list_ids = d_block_ids;
+  opt.list_count = d_block_count;
+  opt.list_stride = ids_stride;
+  return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
+                                       n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
+                                       reinterpret_cast<cudaStream_t>(stream)),
+                 "tensor-core block-list attend");
 }
 
 kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,

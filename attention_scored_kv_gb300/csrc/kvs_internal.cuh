@@ -44,6 +44,15 @@ enum : int32_t {
 constexpr int kCounterInts = 64;
 constexpr int kDepartAt = 32;
 
+// Options of a tensor-core attend launch (all off by default).
+struct AttendOpts {
+  const void* k_new = nullptr;       // fused append of one token per sequence
+  const void* v_new = nullptr;
+  const int32_t* list_ids = nullptr; // block list [n_seqs][list_stride], list_count[n_seqs]
+  const int32_t* list_count = nullptr;
+  int list_stride = 0;
+};
+
 struct Dev {
   // shape
   int32_t L, Hq, Hkv, D, G;

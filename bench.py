@@ -328,6 +328,26 @@ def run_ours(args, world, rank, local):
     a1.record()
     torch.cuda.synchronize()
     attend_us = a0.elapsed_time(a1) * 1e3 / (args.attend_reps * L)
+
+    # ---- Tier-2 re-attend over the blocks the last step kept: graph of L launches
+    reattend = None
+    if lay.attend_kernel == kvs.KERNEL_TENSOR:
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            for l in range(L):
+                cache.attend_blocks(l, Q[1, l], keep_ids, keep_cnt, out=OUT[l])
+        for _ in range(2):
+            gr.replay()
+        torch.cuda.synchronize()
+        r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        r0.record()
+        for _ in range(args.attend_reps):
+            gr.replay()
+        r1.record()
+        torch.cuda.synchronize()
+        reattend_us = r0.elapsed_time(r1) * 1e3 / (args.attend_reps * L)
+        kept = int(keep_cnt.sum().item())
+        assert cache.get_status() == 0, cache.last_error()
     nxt = cache.read_state(kvs.STATE_NEXT_POSITION, 0).cpu().numpy().view(np.int64)
     if wl.h2o_budget_tokens:
         bt = cache.read_state(kvs.STATE_BLOCK_TABLE).cpu().numpy().view(np.int32).reshape(B, lay.max_blocks)
@@ -340,6 +360,19 @@ def run_ours(args, world, rank, local):
     bytes_per_launch = entries * kv_bytes_per_entry(wl)
     hbm, peak_kind = peaks()
     achieved = bytes_per_launch / (attend_us * 1e-6) / 1e9
+    if lay.attend_kernel == kvs.KERNEL_TENSOR:
+        # resident entries of the kept blocks (a sequence's first and last block may be partial)
+        ids_h, cnt_h = keep_ids.cpu().numpy(), keep_cnt.cpu().numpy()
+        rent = 0
+        for s in range(B):
+            nx = int(nxt[s])
+            lo = max(0, nx - wl.window) if wl.window else 0
+            for kb in ids_h[s, : int(cnt_h[s])]:
+                rent += max(0, min(nx, 16 * int(kb) + 16) - max(lo, 16 * int(kb)))
+        rbytes = rent * kv_bytes_per_entry(wl)
+        reattend = {"blocks_kept": kept, "kv_bytes_per_launch": int(rbytes), "launch_us": round(reattend_us, 3),
+                    "kv_gbs": round(rbytes / (reattend_us * 1e-6) / 1e9, 1),
+                    "frac_of_hbm": round(rbytes / (reattend_us * 1e-6) / 1e9 / hbm, 4)}
     traffic = None                      # DRAM bytes per launch measured by ncu, this workload only
     if wl0.name == "e4m3-b16-ctx32768-window4096":
         traffic = profiled_traffic(["attention_scored_kv_gb300/csrc/attend_tc.cu",
@@ -413,6 +446,7 @@ def run_ours(args, world, rank, local):
                      "algorithmic_bytes_per_launch": int(bytes_per_launch)},
         "e2e": {"value": round(e2e_value, 2), "unit": "decode steps/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps},
+        "reattend": reattend,
         "gpu_launches": int(per_step_launches * args.steps),
         "clocks": clocks,
     }

@@ -181,6 +181,24 @@ KVS_API kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_be
                              const void* d_k, const void* d_v, const void* d_q, float* d_out,
                              kvs_stream_t stream);
 
+/* Tier-2 re-attend ("Context views at marginal cost", Tier 2 and Fact 3): decode
+ * attention of one query per head over the cached K and V of a selected subset only.
+ * The subset is the resident entries of the listed blocks, for example the keep_ids
+ * that kvs_select_blocks returns.  d_block_ids: [n_seqs][ids_stride] int32 block ids
+ * (each listed once); d_block_count: [n_seqs] int32, the first count entries of a row
+ * are used (clamped to [0, ids_stride]); both device memory.  d_q, d_out as in
+ * kvs_decode_attend.  Softmax over the subset; no mass or score is written.  Listed
+ * blocks must be resident: with every listed entry outside the resident range the
+ * row has no entry and its output is not finite.  A block id out of range, or (H2O)
+ * not resident, is reported as KVS_ERR_STATE by kvs_get_status and its entries are
+ * left out.
+ * Errors: KVS_ERR_UNSUPPORTED unless the context uses the tensor-core attend;
+ * KVS_ERR_EMPTY_CACHE as kvs_decode_attend; KVS_ERR_INVALID_ARGUMENT for missing
+ * buffers, ids_stride < 1 or unaligned q / out. */
+KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                             const int32_t* d_block_ids, int32_t ids_stride, const int32_t* d_block_count,
+                             const void* d_q, float* d_out, kvs_stream_t stream);
+
 /* kvs_decode_attend without any exchange area from the caller.  No page counterpart:
  * this is a deployment variant, not a step of the method.
  *

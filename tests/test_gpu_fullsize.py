@@ -5,7 +5,7 @@ where the context allows, and accumulate_select, as bench.py's step does.  The o
 follows a sample of the sequences from their first token:
 - 35B bf16 (8 x 4096) and FP8 (16 x 32768, window 4096): every output row, the
   masses, the score tables, the selection and the stored codes of the sampled
-  sequences, every step.
+  sequences, every step; for FP8 also the Tier-2 re-attend over the kept blocks.
 - Ragged FP8 with H2O (64 sequences up to 32768, budget 2048, eviction applied): the
   same for one sampled sequence over the first steps, from the full-context first
   step to the evicted steady state.
@@ -56,6 +56,19 @@ def test_fullsize_e4m3_b16_ctx32768_window4096():
     wl = dataclasses.replace(workloads.get("e4m3-b16-ctx32768-window4096"), steps=3)
     run = _bench_path_check(wl, oseqs=[0, 9], steps=3)
     assert run.cache.layout().attend_kernel == kvs.KERNEL_TENSOR
+    # Tier-2 re-attend of a new query over the blocks a selection keeps (k = 64 of 257)
+    lay = run.cache.layout()
+    ids, cnt = run.cache.select_blocks(wl.keep_k(257), keep_capacity=lay.max_blocks)
+    worst = 0.0
+    for l in (0, wl.num_layers - 1):
+        q = run.inp.step_q(l, wl.steps + 5)
+        got = run.cache.attend_blocks(l, q, ids, cnt)
+        qf = workloads.as_f64(q)
+        for i, s in enumerate(run.oseqs):
+            ref, _, _ = run.oracle.attend_blocks(l, i, qf[s], ids[s, : int(cnt[s])].cpu().numpy())
+            worst = max(worst, harness.rel_err_rows(got[s].double().cpu().numpy(), ref))
+    assert worst <= harness.OUT_TOL[wl.kv_format], worst
+    assert run.cache.get_status() == 0
 
 
 def test_fullsize_e4m3_b64_ragged_h2o2048():

@@ -172,6 +172,76 @@ def test_accumulate_select_is_bitwise_the_two_calls(name, kind, krule):
     assert a.get_status() == 0 and b.get_status() == 0
 
 
+def _reattend_check(run, keep_ids, keep_cnt, t_query):
+    """attend_blocks over the kept blocks of every oracle sequence against the oracle's
+    Tier-2 re-attend, with a query the cache has not seen; returns the worst error and
+    the largest change from full attention (reported, not a bar)."""
+    wl = run.wl
+    worst, moved = 0.0, 0.0
+    for l in range(wl.num_layers):
+        q = run.inp.step_q(l, t_query)
+        got = run.cache.attend_blocks(l, q, keep_ids, keep_cnt)
+        full = run.cache.decode_attend(l, q)     # note: refreshes this layer's step masses
+        qf = workloads.as_f64(q)
+        for i, s in enumerate(run.oseqs):
+            blocks = keep_ids[s, : int(keep_cnt[s])].cpu().numpy()
+            ref, _, pos = run.oracle.attend_blocks(l, i, qf[s], blocks)
+            worst = max(worst, harness.rel_err_rows(got[s].double().cpu().numpy(), ref))
+            moved = max(moved, float((got[s] - full[s]).abs().max()))
+    return worst, moved
+
+
+@pytest.mark.parametrize("name", ["e4m3-b16-window", "bf16", "bf16-hkv8", "e4m3-h2o"])
+def test_attend_blocks_against_oracle(name):
+    """Tier-2 re-attend over the blocks a selection kept, against the oracle, on the
+    tensor-core kernel (window, no window, 8 KV heads, H2O pages)."""
+    wl = dataclasses.replace(SMALL[name], steps=min(SMALL[name].steps, 4))
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    for t in range(wl.steps - 1):
+        run.decode_step(select=False)
+        run.select()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ncand = run.candidate_counts() if not wl.h2o_budget_tokens else [lay.max_blocks] * wl.batch
+    ks = torch.tensor([max(1, wl.keep_k(int(n)) // 2) for n in ncand], dtype=torch.int32, device="cuda")
+    ids, cnt = run.cache.select_blocks(ks, keep_capacity=lay.max_blocks)
+    # the oracle keeps its own residency; re-attend reads both sides' kept blocks
+    worst, moved = _reattend_check(run, ids, cnt, t_query=wl.steps)
+    assert worst <= harness.OUT_TOL[wl.kv_format], worst
+    assert moved > 0.0                           # a strict subset changes the output
+    assert run.cache.get_status() == 0, run.cache.last_error()
+
+
+def test_attend_blocks_over_every_block_is_full_attention():
+    wl = dataclasses.replace(SMALL["e4m3-window"], steps=2)
+    run = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ids, cnt = run.cache.select_blocks(10 ** 6, keep_capacity=lay.max_blocks)   # keeps all
+    for l in range(wl.num_layers):
+        q = run.inp.step_q(l, 5)
+        full = run.cache.decode_attend(l, q)
+        got = run.cache.attend_blocks(l, q, ids, cnt)
+        assert float((got - full).abs().max()) <= 1e-5
+
+
+def test_attend_blocks_reports_a_bad_block_id():
+    wl = dataclasses.replace(SMALL["e4m3-window"], steps=2)
+    run = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ids, cnt = run.cache.select_blocks(4, keep_capacity=lay.max_blocks)
+    bad = ids.clone()
+    bad[0, 0] = lay.max_blocks + 7                # out of range: reported, left out
+    run.cache.attend_blocks(0, run.inp.step_q(0, 5), bad, cnt)
+    assert run.cache.get_status() == kvs._abi.ERR_STATE
+    run.cache.clear_error()
+    assert run.cache.get_status() == 0
+
+
 @pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-h2o"])
 def test_general_kernel_on_tensor_shapes(name):
     wl = SMALL[name]
