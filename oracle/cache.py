@@ -36,7 +36,16 @@ from . import attention, e4m3, selection
 
 
 class ScoreTables:
-    """Cumulative and EMA tables of one sequence, per token and per block."""
+    """Cumulative and EMA tables of one sequence, per token and per block, plus two
+    block scores summed over the block's entries:
+
+    - s_blk: sum over steps and entries of the entry scores x, i.e. the accumulated
+      attention summed over heads, layers and the block's tokens (H2O's score, "Context
+      Optimization", H2O > How It Works step 1, at block granularity);
+    - t_blk: the same sum for the latest step only (TOVA's latest-query weight, summed
+      over heads and layers rather than averaged: the same ranking; "Context views at
+      marginal cost", the per-system reductions).
+    """
 
     def __init__(self, max_positions, block_tokens=16, ema_decay=0.9):
         self.block_tokens = block_tokens
@@ -46,6 +55,8 @@ class ScoreTables:
         self.e_tok = np.zeros(max_positions)
         self.c_blk = np.zeros(nb)
         self.e_blk = np.zeros(nb)
+        self.s_blk = np.zeros(nb)
+        self.t_blk = np.zeros(nb)
         self.steps = 0
 
     def update(self, tracked_positions, x_tok, y_blk):
@@ -64,6 +75,11 @@ class ScoreTables:
         self.e_tok[:n] = d * self.e_tok[:n] + (1.0 - d) * x
         self.c_blk[:nb] = self.c_blk[:nb] + y
         self.e_blk[:nb] = d * self.e_blk[:nb] + (1.0 - d) * y
+        t = np.zeros(nb)
+        for j in range(n):                          # sum of x over each block's entries
+            t[j // self.block_tokens] += x[j]
+        self.s_blk[:nb] = self.s_blk[:nb] + t
+        self.t_blk[:nb] = t
         self.steps += 1
 
 
@@ -228,10 +244,14 @@ class OracleKV:
 
     # ---------------------------------------------------------------- a5 select
     def select(self, seq, k, score_kind="cumulative", protect=False, apply=False):
-        """Kept block ids (ascending).  protect: H2O sink/recent protection with k as
-        the block budget; apply: evict the unkept blocks (H2O mode only)."""
+        """Kept block ids (ascending) by a block score: "cumulative" (C of the block
+        mass), "ema", "token_sum" (H2O: accumulated entry scores summed over the block)
+        or "tova" (the latest step's entry scores summed over the block; keeping the top
+        k is evicting the argmin until k remain).  protect: H2O sink/recent protection
+        with k as the block budget; apply: evict the unkept blocks (H2O mode only)."""
         cand = self.resident_block_ids(seq)
-        table = self.scores[seq].c_blk if score_kind == "cumulative" else self.scores[seq].e_blk
+        table = {"cumulative": self.scores[seq].c_blk, "ema": self.scores[seq].e_blk,
+                 "token_sum": self.scores[seq].s_blk, "tova": self.scores[seq].t_blk}[score_kind]
         scores = {c: table[c] for c in cand}
         nxt = int(self.next_position[0, seq])
         if protect:
