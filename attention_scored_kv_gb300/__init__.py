@@ -14,13 +14,14 @@ import torch
 
 from . import _abi
 from ._abi import (  # noqa: F401
-    F32, BF16, E4M3, SCORE_CUMULATIVE, SCORE_EMA, KERNEL_AUTO, KERNEL_GENERAL, KERNEL_TENSOR,
+    F32, BF16, E4M3, SCORE_CUMULATIVE, SCORE_EMA, SCORE_TOKEN_SUM, SCORE_TOVA, KERNEL_AUTO, KERNEL_GENERAL,
+    KERNEL_TENSOR,
     MODE_NONE, MODE_WINDOW, MODE_H2O, SELECT_PROTECT, SELECT_APPLY, Config, Layout,
 )
 from ._abi import (  # noqa: F401
     STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
     STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
-    STATE_BLOCK_TABLE,
+    STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK,
 )
 
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}

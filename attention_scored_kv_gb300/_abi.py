@@ -14,7 +14,7 @@ STATUS_NAMES = {0: "OK", 1: "INVALID_ARGUMENT", 2: "CAPACITY", 3: "EMPTY_CACHE",
 # kvs_dtype
 F32, BF16, E4M3 = 0, 1, 2
 # kvs_score_kind
-SCORE_CUMULATIVE, SCORE_EMA = 0, 1
+SCORE_CUMULATIVE, SCORE_EMA, SCORE_TOKEN_SUM, SCORE_TOVA = 0, 1, 2, 3
 # kvs_kernel
 KERNEL_AUTO, KERNEL_GENERAL, KERNEL_TENSOR = 0, 1, 2
 # kvs_mode
@@ -24,7 +24,7 @@ SELECT_PROTECT, SELECT_APPLY = 1, 2
 # kvs_state_item
 (STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
  STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
- STATE_BLOCK_TABLE) = range(14)
+ STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK) = range(16)
 
 
 class Config(ctypes.Structure):

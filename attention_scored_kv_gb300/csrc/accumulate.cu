@@ -15,19 +15,22 @@ __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
   const int i = blockIdx.x * kBlocksPerCta + (threadIdx.x >> 4);
   const int j = threadIdx.x & 15;
+  double x = 0.0;
+  int32_t k = -1;
   if (i < sb.n) {
     int32_t page;
-    const int32_t k = block_at(d, s, sb, i, &page);
+    k = block_at(d, s, sb, i, &page);
     const int64_t p = (int64_t)k * kBlock + j;
     if (p >= sb.lo && p < sb.next) {
       int32_t slot;
       page = page_of(d, s, p, &slot);
-      update_entry(d, s, p, page, slot, step);
+      x = update_entry(d, s, p, page, slot, step);
     }
-    if (j == 0) {
-      double c_new, e_new;
-      update_block(d, s, k, step, &c_new, &e_new);
-    }
+  }
+  const double xsum = block_entry_sum(x);        // the block's 16 entries are 16 lanes
+  if (i < sb.n && j == 0) {
+    double c_new, e_new;
+    update_block(d, s, k, step, xsum, &c_new, &e_new);
   }
   __syncthreads();
   if (threadIdx.x == 0) {

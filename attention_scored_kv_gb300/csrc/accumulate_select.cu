@@ -54,19 +54,22 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
 
   // ---- accumulate, exactly as the accumulate kernel
   const int ib = blockIdx.x * kBlocksPerCta + (tid >> 4), j = tid & 15;
+  double x = 0.0;
+  int32_t kb = -1;
   if (ib < sb.n) {
     int32_t page;
-    const int32_t k = block_at(d, s, sb, ib, &page);
-    const int64_t p = (int64_t)k * kBlock + j;
+    kb = block_at(d, s, sb, ib, &page);
+    const int64_t p = (int64_t)kb * kBlock + j;
     if (p >= sb.lo && p < sb.next) {
       int32_t slot;
       page = page_of(d, s, p, &slot);
-      update_entry(d, s, p, page, slot, step);
+      x = update_entry(d, s, p, page, slot, step);
     }
-    if (j == 0) {
-      double c_new, e_new;
-      update_block(d, s, k, step, &c_new, &e_new);
-    }
+  }
+  const double xsum = block_entry_sum(x);        // the block's 16 entries are 16 lanes
+  if (ib < sb.n && j == 0) {
+    double c_new, e_new;
+    update_block(d, s, kb, step, xsum, &c_new, &e_new);
   }
   __syncthreads();
   if (tid == 0) {

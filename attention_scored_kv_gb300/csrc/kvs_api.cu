@@ -44,7 +44,7 @@ struct Plan {
   // region offsets
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
-  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, steps, acc_tickets;
+  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, steps, acc_tickets;
   size_t partials, part_ml, counters, logits, err;
 };
 
@@ -152,6 +152,8 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->last_tok = take(B * P * 4);
   p->c_blk = take(B * MB * 8);
   p->e_blk = take(B * MB * 8);
+  p->s_blk = take(B * MB * 8);
+  p->t_blk = take(B * MB * 8);
   p->last_blk = take(B * MB * 4);
   p->steps = take(B * 4);
   p->acc_tickets = take(B * 4);
@@ -297,6 +299,8 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.last_tok = reinterpret_cast<int32_t*>(w + p.last_tok);
   d.c_blk = reinterpret_cast<double*>(w + p.c_blk);
   d.e_blk = reinterpret_cast<double*>(w + p.e_blk);
+  d.s_blk = reinterpret_cast<double*>(w + p.s_blk);
+  d.t_blk = reinterpret_cast<double*>(w + p.t_blk);
   d.last_blk = reinterpret_cast<int32_t*>(w + p.last_blk);
   d.steps = reinterpret_cast<int32_t*>(w + p.steps);
   d.acc_tickets = reinterpret_cast<int32_t*>(w + p.acc_tickets);
@@ -548,8 +552,8 @@ kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, co
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_range(ctx, seq_begin, n_seqs);
   if (st != KVS_OK) return st;
-  if (score_kind != KVS_SCORE_CUMULATIVE && score_kind != KVS_SCORE_EMA)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE or EMA");
+  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
   if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
   if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
@@ -575,8 +579,8 @@ kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_range(ctx, seq_begin, n_seqs);
   if (st != KVS_OK) return st;
-  if (score_kind != KVS_SCORE_CUMULATIVE && score_kind != KVS_SCORE_EMA)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE or EMA");
+  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
   if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
   if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
@@ -622,7 +626,7 @@ size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
     case KVS_STATE_TOKEN_MASS: return slots * 4;
     case KVS_STATE_BLOCK_MASS: return B * MB * 4;
     case KVS_STATE_C_TOKEN: case KVS_STATE_E_TOKEN: return B * ctx->cfg.max_positions * 8;
-    case KVS_STATE_C_BLOCK: case KVS_STATE_E_BLOCK: return B * MB * 8;
+    case KVS_STATE_C_BLOCK: case KVS_STATE_E_BLOCK: case KVS_STATE_S_BLOCK: case KVS_STATE_T_BLOCK: return B * MB * 8;
     case KVS_STATE_STEPS: return B * 4;
     case KVS_STATE_BLOCK_TABLE: return B * MB * 4;
     default: return 0;
@@ -651,10 +655,11 @@ kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst
     case KVS_STATE_BLOCK_MASS: src = d.blk_mass + layer * d.blk_layer_elems; break;
     case KVS_STATE_C_TOKEN: src = d.c_tok; break;
     case KVS_STATE_C_BLOCK: src = d.c_blk; break;
+    case KVS_STATE_S_BLOCK: src = d.s_blk; break;
     case KVS_STATE_STEPS: src = d.steps; break;
     case KVS_STATE_BLOCK_TABLE: src = d.block_table; break;
-    case KVS_STATE_E_TOKEN: case KVS_STATE_E_BLOCK:
-      return cuda_ok(ctx, launch_read_ema(d, what, static_cast<double*>(d_dst), cs), "read EMA");
+    case KVS_STATE_E_TOKEN: case KVS_STATE_E_BLOCK: case KVS_STATE_T_BLOCK:
+      return cuda_ok(ctx, launch_read_ema(d, what, static_cast<double*>(d_dst), cs), "read score");
     default: return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "state item %d", what);
   }
   return cuda_ok(ctx, cudaMemcpyAsync(d_dst, src, n, cudaMemcpyDeviceToDevice, cs), "read state");

@@ -79,6 +79,7 @@ struct Dev {
   int32_t* free_top;      // [1]
   double* c_tok; double* e_tok; int32_t* last_tok;   // [max_seqs][max_positions]
   double* c_blk; double* e_blk; int32_t* last_blk;   // [max_seqs][max_blocks]
+  double* s_blk; double* t_blk;                      // [max_seqs][max_blocks] summed over entries
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
   float* partials;        // [records][Hq][D] partial output rows, records = kGridMax + max_seqs

@@ -26,9 +26,9 @@ __device__ __forceinline__ double decayed(double e, int32_t last, int32_t step, 
   return e * pow(dec, (double)gap);
 }
 
-// Entry p of sequence s, stored in (page, slot), at step `step`.
-__device__ __forceinline__ void update_entry(const Dev& d, int s, int64_t p, int32_t page, int32_t slot,
-                                             int32_t step) {
+// Entry p of sequence s, stored in (page, slot), at step `step`; returns its score x.
+__device__ __forceinline__ double update_entry(const Dev& d, int s, int64_t p, int32_t page, int32_t slot,
+                                               int32_t step) {
   double x = 0.0;
   for (int l = 0; l < d.L; ++l)
     x += (double)d.tok_mass[(size_t)l * d.slot_layer_elems + (size_t)page * kBlock + slot];
@@ -38,12 +38,23 @@ __device__ __forceinline__ void update_entry(const Dev& d, int s, int64_t p, int
   d.c_tok[t] += x;
   d.e_tok[t] = d.ema_decay * e_prev + (1.0 - d.ema_decay) * x;
   d.last_tok[t] = step;
+  return x;
 }
 
-// Block k of sequence s at step `step`; returns the new cumulative score in *c_new and
-// the new EMA in *e_new.
-__device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int32_t step, double* c_new,
-                                             double* e_new) {
+// Sum of the entry scores x of one block's 16 entries, held by 16 consecutive lanes
+// (lane & 15 = entry; entries left out contribute 0).  Every lane of the warp calls it;
+// lanes of the block get the sum.  Added in a fixed tree order.
+__device__ __forceinline__ double block_entry_sum(double x) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+
+// Block k of sequence s at step `step`, whose entries' scores sum to xsum; returns the
+// new cumulative score in *c_new and the new EMA in *e_new.  The token-sum score
+// (H2O) accumulates xsum, and the TOVA score is xsum.
+__device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int32_t step, double xsum,
+                                             double* c_new, double* e_new) {
   float y = 0.f;
   for (int l = 0; l < d.L; ++l)
     y = fmaxf(y, d.blk_mass[(size_t)l * d.blk_layer_elems + (size_t)s * d.max_blocks + k]);
@@ -54,6 +65,8 @@ __device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int
   const double e = d.ema_decay * e_prev + (1.0 - d.ema_decay) * (double)y;
   d.c_blk[t] = c;
   d.e_blk[t] = e;
+  d.s_blk[t] += xsum;
+  d.t_blk[t] = xsum;
   d.last_blk[t] = step;
   *c_new = c;
   *e_new = e;

@@ -24,7 +24,8 @@ __device__ __forceinline__ bool protected_block(const Dev& d, int32_t k, int64_t
 }
 
 // Key of the i-th resident block of sequence s (its id and page to *kid, *page): the
-// cumulative score, or the EMA as of step steps_now - 1, or ~0 when protected.
+// cumulative score, the EMA as of step steps_now - 1, the token sum, or the TOVA score
+// of step steps_now - 1 (0 for a block that step did not update); ~0 when protected.
 // L2ONLY reads the tables through L2 only (they were just written by other CTAs).
 template <bool L2ONLY>
 __device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlocks& sb, int i, int kind, bool protect,
@@ -36,6 +37,12 @@ __device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlock
   double v;
   if (kind == KVS_SCORE_CUMULATIVE) {
     v = L2ONLY ? __ldcg(d.c_blk + t) : d.c_blk[t];
+  } else if (kind == KVS_SCORE_TOKEN_SUM) {
+    v = L2ONLY ? __ldcg(d.s_blk + t) : d.s_blk[t];
+  } else if (kind == KVS_SCORE_TOVA) {
+    const int32_t last = L2ONLY ? __ldcg(d.last_blk + t) : d.last_blk[t];
+    const double tv = L2ONLY ? __ldcg(d.t_blk + t) : d.t_blk[t];
+    v = last == steps_now - 1 ? tv : 0.0;
   } else {
     const int32_t last = L2ONLY ? __ldcg(d.last_blk + t) : d.last_blk[t];
     const double e = L2ONLY ? __ldcg(d.e_blk + t) : d.e_blk[t];

@@ -35,6 +35,8 @@ __global__ void reset_kernel(Dev d, int seq_begin) {
   for (int k = threadIdx.x; k < d.max_blocks; k += blockDim.x) {
     d.c_blk[blk_base + k] = 0.0;
     d.e_blk[blk_base + k] = 0.0;
+    d.s_blk[blk_base + k] = 0.0;
+    d.t_blk[blk_base + k] = 0.0;
     d.last_blk[blk_base + k] = -1;
   }
   if (d.mode == KVS_MODE_H2O) {
@@ -120,6 +122,11 @@ cudaError_t launch_read_ema(const Dev& d, int what, double* dst, cudaStream_t st
     const size_t n = (size_t)d.max_seqs * d.max_positions;
     read_ema_kernel<<<grid_for(n), 256, 0, st>>>(d.e_tok, d.last_tok, d.steps, d.max_positions,
                                                  d.max_seqs, d.ema_decay, dst);
+  } else if (what == KVS_STATE_T_BLOCK) {
+    // the latest step's score: the stored value where the block was updated in the last
+    // step, else 0 (decay 0: 0^0 = 1, 0^gap = 0)
+    const size_t n = (size_t)d.max_seqs * d.max_blocks;
+    read_ema_kernel<<<grid_for(n), 256, 0, st>>>(d.t_blk, d.last_blk, d.steps, d.max_blocks, d.max_seqs, 0.0, dst);
   } else {
     const size_t n = (size_t)d.max_seqs * d.max_blocks;
     read_ema_kernel<<<grid_for(n), 256, 0, st>>>(d.e_blk, d.last_blk, d.steps, d.max_blocks,

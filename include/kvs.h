@@ -80,7 +80,18 @@ typedef enum {
 
 typedef enum { KVS_F32 = 0, KVS_BF16 = 1, KVS_E4M3 = 2 } kvs_dtype;
 
-typedef enum { KVS_SCORE_CUMULATIVE = 0, KVS_SCORE_EMA = 1 } kvs_score_kind;
+/* Block scores a selection can rank by ("Per-Head Attention as a Scoring Signal",
+ * Combined placement decision; "Context views at marginal cost", per-system
+ * reductions):
+ *   CUMULATIVE  sum over steps of the block mass (max over layers and heads of the
+ *               in-block weight sum)
+ *   EMA         its exponential moving average
+ *   TOKEN_SUM   H2O: sum over steps of the entry scores (weights summed over heads and
+ *               layers) summed over the block's entries
+ *   TOVA        the latest step's entry scores summed over the block's entries (the
+ *               latest query's weight; keeping the top k evicts the argmin blocks) */
+typedef enum { KVS_SCORE_CUMULATIVE = 0, KVS_SCORE_EMA = 1, KVS_SCORE_TOKEN_SUM = 2,
+               KVS_SCORE_TOVA = 3 } kvs_score_kind;
 
 /* Attend kernel choice: AUTO takes the tensor-core kernel when the shape allows it
  * (head_dim 128, 8 query heads per KV head, bf16 inputs, bf16 or E4M3 storage, and
@@ -290,7 +301,9 @@ typedef enum {
   KVS_STATE_E_BLOCK = 11,
   KVS_STATE_STEPS = 12,      /* [max_seqs] int32 accumulate steps done */
   KVS_STATE_BLOCK_TABLE = 13,/* [max_seqs][max_blocks] int32 page of each block, -1 = none */
-  KVS_STATE_COUNT = 14
+  KVS_STATE_S_BLOCK = 14,    /* [max_seqs][max_blocks] float64 TOKEN_SUM block score */
+  KVS_STATE_T_BLOCK = 15,    /* [max_seqs][max_blocks] float64 TOVA block score of the last step */
+  KVS_STATE_COUNT = 16
 } kvs_state_item;
 
 KVS_API size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what);

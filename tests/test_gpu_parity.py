@@ -122,6 +122,9 @@ def test_fused_append_attend_from_an_empty_cache():
 
 @pytest.mark.parametrize("name,kind,krule", [
     ("e4m3-b16-window", kvs.SCORE_CUMULATIVE, "per-seq"),
+    ("e4m3-b16-window", kvs.SCORE_TOVA, "per-seq"),
+    ("bf16", kvs.SCORE_TOKEN_SUM, 3),
+    ("e4m3-h2o", kvs.SCORE_TOVA, "h2o"),
     ("bf16", kvs.SCORE_EMA, 3),
     ("e4m3-nowindow", kvs.SCORE_EMA, 0),
     ("e4m3-window", kvs.SCORE_CUMULATIVE, 10 ** 6),
@@ -161,7 +164,8 @@ def test_accumulate_select_is_bitwise_the_two_calls(name, kind, krule):
             n = int(outs[0][1][s])
             assert torch.equal(outs[0][0][s, :n], outs[1][0][s, :n]), (t, s)
     a, b = runs[0].cache, runs[1].cache
-    for n in (kvs.STATE_C_TOKEN, kvs.STATE_E_TOKEN, kvs.STATE_C_BLOCK, kvs.STATE_E_BLOCK, kvs.STATE_STEPS):
+    for n in (kvs.STATE_C_TOKEN, kvs.STATE_E_TOKEN, kvs.STATE_C_BLOCK, kvs.STATE_E_BLOCK, kvs.STATE_STEPS,
+              kvs.STATE_S_BLOCK, kvs.STATE_T_BLOCK):
         assert torch.equal(a.read_state(n).cpu(), b.read_state(n).cpu()), n
     if h2o:
         # the same blocks stay resident; which free page a block gets depends on the order
@@ -170,6 +174,39 @@ def test_accumulate_select_is_bitwise_the_two_calls(name, kind, krule):
         btb = b.read_state(kvs.STATE_BLOCK_TABLE).cpu().view(torch.int32)
         assert torch.equal(bta >= 0, btb >= 0)
     assert a.get_status() == 0 and b.get_status() == 0
+
+
+@pytest.mark.parametrize("name", ["e4m3-window", "bf16", "e4m3-h2o"])
+def test_token_sum_and_tova_scores_against_oracle(name):
+    """The summed block scores (H2O token sum, TOVA latest weight) and the selections by
+    them, against the oracle, every step (window: blocks leave it; H2O: eviction by the
+    cumulative score as the workload says, then TOVA and token-sum selections read
+    only)."""
+    wl = dataclasses.replace(SMALL[name], steps=min(SMALL[name].steps, 10))
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    lay = run.cache.layout()
+    for t in range(wl.steps):
+        run.decode_step(select=False)
+        sv = harness.StateView(run.cache, wl)
+        sb = sv.raw(kvs.STATE_S_BLOCK).view(np.float64).reshape(wl.batch, lay.max_blocks)
+        tb = sv.raw(kvs.STATE_T_BLOCK).view(np.float64).reshape(wl.batch, lay.max_blocks)
+        for i, s in enumerate(run.oseqs):
+            sc = run.oracle.scores[i]
+            n = len(sc.s_blk)
+            assert np.max(np.abs(sb[s, :n] - sc.s_blk)) <= harness.SCORE_TOL
+            assert np.max(np.abs(tb[s, :n] - sc.t_blk)) <= harness.SCORE_TOL
+        for kind, table, okind in ((kvs.SCORE_TOVA, "t_blk", "tova"), (kvs.SCORE_TOKEN_SUM, "s_blk", "token_sum")):
+            ncand = run.candidate_counts() if not wl.h2o_budget_tokens else \
+                [len(run.oracle.resident_block_ids(i)) for i in range(wl.batch)]
+            ks = torch.tensor([max(1, int(n) // 2) for n in ncand], dtype=torch.int32, device="cuda")
+            ids, cnt = run.cache.select_blocks(ks, score_kind=kind, keep_capacity=lay.max_blocks)
+            ids, cnt = ids.cpu().numpy(), cnt.cpu().numpy()
+            gpu = {s: list(ids[s, :cnt[s]]) for s in range(wl.batch)}
+            ora = {s: run.oracle.select(i, int(ks[s].item()), score_kind=okind) for i, s in enumerate(run.oseqs)}
+            harness.check_selection(run, (gpu, ora), table=table)
+        run.select()                                  # the workload's own rule (H2O: evicts)
+    assert run.cache.get_status() == 0, run.cache.last_error()
 
 
 def _reattend_check(run, keep_ids, keep_cnt, t_query):
