@@ -47,10 +47,17 @@ class ScoreTables:
       marginal cost", the per-system reductions).
     """
 
-    def __init__(self, max_positions, block_tokens=16, ema_decay=0.9):
+    def __init__(self, max_positions, block_tokens=16, ema_decay=0.9, traj_len=0, profile_layers=()):
         self.block_tokens = block_tokens
         self.d = float(ema_decay)
         nb = -(-max_positions // block_tokens)
+        # side-car views ("Context views at marginal cost", Tier 1): a ring of the last
+        # traj_len steps' t_blk ("when was the span hot"), and per profiled layer the
+        # sum over steps of that layer's block mass ("within layer L")
+        self.traj_len = traj_len
+        self.traj = np.zeros((traj_len, nb))
+        self.profile_layers = tuple(profile_layers)
+        self.prof = np.zeros((len(self.profile_layers), nb))
         self.c_tok = np.zeros(max_positions)
         self.e_tok = np.zeros(max_positions)
         self.c_blk = np.zeros(nb)
@@ -59,7 +66,17 @@ class ScoreTables:
         self.t_blk = np.zeros(nb)
         self.steps = 0
 
-    def update(self, tracked_positions, x_tok, y_blk):
+    def trajectory(self):
+        """[nb][traj_len]: t_blk of the last traj_len steps, oldest first (0 before the
+        first step)."""
+        out = np.zeros((self.traj.shape[1], self.traj_len))
+        for j in range(self.traj_len):
+            step = self.steps - self.traj_len + j          # 0-based step index
+            if step >= 0:
+                out[:, j] = self.traj[step % self.traj_len]
+        return out
+
+    def update(self, tracked_positions, x_tok, y_blk, layer_blk=None):
         """One step.  x_tok: float64 array over positions 0..tracked_positions-1 with
         the step's token scores (0 where nothing attended); y_blk: float64 array over
         the blocks holding a tracked position, likewise.  Every tracked entry is
@@ -80,6 +97,12 @@ class ScoreTables:
             t[j // self.block_tokens] += x[j]
         self.s_blk[:nb] = self.s_blk[:nb] + t
         self.t_blk[:nb] = t
+        if self.traj_len:
+            self.traj[self.steps % self.traj_len, :] = 0.0
+            self.traj[self.steps % self.traj_len, :nb] = t
+        for i, l in enumerate(self.profile_layers):
+            for k, m in layer_blk[l].items():
+                self.prof[i, k] += m
         self.steps += 1
 
 
@@ -88,7 +111,8 @@ class OracleKV:
 
     def __init__(self, *, num_layers, num_q_heads, num_kv_heads, head_dim, num_seqs,
                  max_positions, kv_format="bf16", window=0, h2o_budget_tokens=0,
-                 h2o_sink_tokens=4, h2o_recent_frac=0.25, ema_decay=0.9, block_tokens=16):
+                 h2o_sink_tokens=4, h2o_recent_frac=0.25, ema_decay=0.9, block_tokens=16, traj_len=0,
+                 profile_layers=()):
         if num_q_heads % num_kv_heads:
             raise ValueError("num_q_heads must be a multiple of num_kv_heads")
         if window < 0:
@@ -126,7 +150,8 @@ class OracleKV:
             self.k_vals = np.zeros(shape, dtype=np.float32)
             self.v_vals = np.zeros(shape, dtype=np.float32)
         self.resident_blocks = [set() for _ in range(num_seqs)]      # H2O mode only
-        self.scores = [ScoreTables(max_positions, block_tokens, ema_decay) for _ in range(num_seqs)]
+        self.scores = [ScoreTables(max_positions, block_tokens, ema_decay, traj_len, profile_layers)
+                       for _ in range(num_seqs)]
         self._tok_mass = {}      # (l, b) -> (positions, token mass) of the latest attend
         self._blk_mass = {}      # (l, b) -> {block: mass} of the latest attend
         self._attended = set()   # (l, b) attended since the last accumulate
@@ -230,6 +255,7 @@ class OracleKV:
             n = nxt.pop()
             x_tok = np.zeros(n)
             y_blk = np.zeros(-(-n // self.block))
+            layer_blk = {}
             for l in range(self.L):
                 if (l, b) not in self._attended:
                     raise ValueError("layer %d of sequence %d was not attended this step" % (l, b))
@@ -238,9 +264,19 @@ class OracleKV:
                 x_tok[pos] += tau                      # sum over layers
                 for k, m in self._blk_mass[(l, b)].items():
                     y_blk[k] = max(y_blk[k], m)        # max over layers
-            self.scores[b].update(n, x_tok, y_blk)
+                layer_blk[l] = self._blk_mass[(l, b)]
+            self.scores[b].update(n, x_tok, y_blk, layer_blk)
             result[b] = (x_tok, y_blk)
         return result
+
+    # ---------------------------------------------------------------- side-car views
+    def filter_blocks(self, seq, score_kind, theta):
+        """Threshold view ("Context views at marginal cost", Tier 1: a view is a filter
+        of the kept table, a_s > theta): the resident blocks whose score exceeds theta,
+        ascending."""
+        table = {"cumulative": self.scores[seq].c_blk, "ema": self.scores[seq].e_blk,
+                 "token_sum": self.scores[seq].s_blk, "tova": self.scores[seq].t_blk}[score_kind]
+        return [c for c in self.resident_block_ids(seq) if table[c] > theta]
 
     # ---------------------------------------------------------------- a5 select
     def select(self, seq, k, score_kind="cumulative", protect=False, apply=False):
