@@ -21,7 +21,7 @@ from ._abi import (  # noqa: F401
 from ._abi import (  # noqa: F401
     STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
     STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
-    STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK,
+    STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE,
 )
 
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}
@@ -230,6 +230,44 @@ class KVCache:
         self._check(lib().kvs_accumulate_select(self._ctx, seq_begin, n, kp, ku, score_kind, flags, _ptr(keep_ids),
                                                 cap, _ptr(keep_count), _stream(stream)))
         return keep_ids, keep_count
+
+    def filter_blocks(self, theta, seq_begin=0, n_seqs=None, score_kind=SCORE_CUMULATIVE, capacity=None,
+                      ids=None, count=None, stream=None):
+        """Resident blocks whose score exceeds theta.  Returns (ids [n_seqs, capacity]
+        int32, count [n_seqs] int32), ids ascending."""
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        cap = self.layout().max_blocks if capacity is None else capacity
+        if ids is None:
+            ids = torch.full((n, cap), -1, dtype=torch.int32, device=self.device)
+        if count is None:
+            count = torch.zeros(n, dtype=torch.int32, device=self.device)
+        _need(ids, "ids", torch.int32, (n, cap))
+        _need(count, "count", torch.int32, (n,))
+        self._check(lib().kvs_filter_blocks(self._ctx, seq_begin, n, score_kind, float(theta), _ptr(ids), cap,
+                                            _ptr(count), _stream(stream)))
+        return ids, count
+
+    # ---- score snapshot
+    def snapshot_bytes(self, n_seqs):
+        return int(lib().kvs_scores_snapshot_bytes(self._ctx, n_seqs))
+
+    def export_scores(self, seq_begin=0, n_seqs=None, dst=None, stream=None):
+        """The score tables of the range as one uint8 tensor (CUDA unless dst, a
+        contiguous uint8 tensor on the device or in pinned host memory, is given)."""
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        nb = self.snapshot_bytes(n)
+        if dst is None:
+            dst = torch.empty(nb, dtype=torch.uint8, device=self.device)
+        if dst.dtype != torch.uint8 or not dst.is_contiguous() or dst.numel() < nb:
+            raise ValueError("dst must be a contiguous uint8 tensor of at least %d bytes" % nb)
+        self._check(lib().kvs_export_scores(self._ctx, seq_begin, n, _ptr(dst), dst.numel(), _stream(stream)))
+        return dst
+
+    def import_scores(self, src, seq_begin=0, n_seqs=None, stream=None):
+        n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
+        if src.dtype != torch.uint8 or not src.is_contiguous():
+            raise ValueError("src must be a contiguous uint8 tensor")
+        self._check(lib().kvs_import_scores(self._ctx, seq_begin, n, _ptr(src), src.numel(), _stream(stream)))
 
     # ---- inspection
     def read_state(self, what, layer=0, stream=None):

@@ -24,7 +24,7 @@ SELECT_PROTECT, SELECT_APPLY = 1, 2
 # kvs_state_item
 (STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
  STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
- STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK) = range(16)
+ STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE) = range(18)
 
 
 class Config(ctypes.Structure):
@@ -34,7 +34,8 @@ class Config(ctypes.Structure):
         ("window", ctypes.c_int32), ("block_tokens", ctypes.c_int32), ("h2o_budget_tokens", ctypes.c_int32),
         ("h2o_sink_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("spin_limit", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
-        ("reserved_i", ctypes.c_int32 * 5), ("h2o_recent_frac", ctypes.c_double), ("ema_decay", ctypes.c_double),
+        ("traj_len", ctypes.c_int32), ("profile_layers", ctypes.c_uint32), ("reserved_i", ctypes.c_int32 * 3),
+        ("h2o_recent_frac", ctypes.c_double), ("ema_decay", ctypes.c_double),
         ("reserved_d", ctypes.c_double * 2),
     ]
 
@@ -62,6 +63,10 @@ _SIGS = {
     "kvs_accumulate_scores": (_I, [_P, _I, _I, _P]),
     "kvs_select_blocks": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
     "kvs_accumulate_select": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
+    "kvs_filter_blocks": (_I, [_P, _I, _I, _I, ctypes.c_double, _P, _I, _P, _P]),
+    "kvs_scores_snapshot_bytes": (ctypes.c_size_t, [_P, _I]),
+    "kvs_export_scores": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
+    "kvs_import_scores": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
     "kvs_state_bytes": (ctypes.c_size_t, [_P, _I]),
     "kvs_read_state": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
     "kvs_get_layout": (_I, [_P, ctypes.POINTER(Layout)]),

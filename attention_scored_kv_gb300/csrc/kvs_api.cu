@@ -44,7 +44,7 @@ struct Plan {
   // region offsets
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
-  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, steps, acc_tickets;
+  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, traj, prof, steps, acc_tickets;
   size_t partials, part_ml, counters, logits, err;
 };
 
@@ -89,7 +89,12 @@ kvs_status check_config(const kvs_config* c, char* msg, size_t n) {
     put(msg, n, "a bf16 cache needs bf16 inputs (f32 would be rounded)");
     return KVS_ERR_UNSUPPORTED;
   }
-  for (int i = 0; i < 5; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->traj_len < 0 || c->traj_len > 256) { put(msg, n, "traj_len must be in [0, 256]"); return KVS_ERR_INVALID_ARGUMENT; }
+  if ((c->num_layers < 32 && (c->profile_layers >> c->num_layers)) || __builtin_popcount(c->profile_layers) > 4) {
+    put(msg, n, "profile_layers: at most 4 bits, each below num_layers");
+    return KVS_ERR_INVALID_ARGUMENT;
+  }
+  for (int i = 0; i < 3; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
   for (int i = 0; i < 2; ++i) if (c->reserved_d[i] != 0.0) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
   const int mode = c->h2o_budget_tokens > 0 ? KVS_MODE_H2O : (c->window > 0 ? KVS_MODE_WINDOW : KVS_MODE_NONE);
   const bool tc = tc_supported(c->num_q_heads, c->num_kv_heads, c->head_dim, c->kv_dtype, c->in_dtype, c->window, mode);
@@ -154,6 +159,8 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->e_blk = take(B * MB * 8);
   p->s_blk = take(B * MB * 8);
   p->t_blk = take(B * MB * 8);
+  p->traj = take(B * MB * (size_t)c->traj_len * 4);
+  p->prof = take(B * MB * (size_t)__builtin_popcount(c->profile_layers) * 8);
   p->last_blk = take(B * MB * 4);
   p->steps = take(B * 4);
   p->acc_tickets = take(B * 4);
@@ -210,6 +217,59 @@ int64_t seq_block_bound(const kvs_ctx* ctx, int s) {
   if (ctx->plan.mode == KVS_MODE_H2O)
     return std::min<int64_t>(ctx->plan.max_blocks, ctx->h2o_bound[s] + 2);
   return ctx->plan.res_blocks_per_seq;
+}
+
+}  // namespace
+
+namespace {
+
+// Sections of a score snapshot of n sequences starting at seq_begin, in snapshot order,
+// each starting on a 256-byte boundary: the table's first element of seq_begin and the
+// bytes of the n sequences' rows.  Returns the number of sections.
+int snapshot_sections(const kvs_ctx* ctx, int seq_begin, int n, void* ptr[11], size_t bytes[11]) {
+  const Dev& d = ctx->dev;
+  const size_t P = d.max_positions, MB = d.max_blocks, s0 = seq_begin, TL = d.traj_len, NP = d.n_prof;
+  int i = 0;
+  auto add = [&](void* p, size_t b) { ptr[i] = p; bytes[i] = b; ++i; };
+  add(d.c_tok + s0 * P, n * P * 8);
+  add(d.e_tok + s0 * P, n * P * 8);
+  add(d.c_blk + s0 * MB, n * MB * 8);
+  add(d.e_blk + s0 * MB, n * MB * 8);
+  add(d.s_blk + s0 * MB, n * MB * 8);
+  add(d.t_blk + s0 * MB, n * MB * 8);
+  add(d.prof + s0 * MB * NP, n * MB * NP * 8);
+  add(d.traj + s0 * MB * TL, n * MB * TL * 4);
+  add(d.last_tok + s0 * P, n * P * 4);
+  add(d.last_blk + s0 * MB, n * MB * 4);
+  add(d.steps + s0, (size_t)n * 4);
+  return i;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+kvs_status snapshot_copy(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* buf, size_t buf_bytes, bool out,
+                         kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  const size_t need = kvs_scores_snapshot_bytes(ctx, n_seqs);
+  if (!buf || buf_bytes < need) return fail(ctx, KVS_ERR_CAPACITY, "snapshot needs %zu bytes", need);
+  void* ptr[11];
+  size_t bytes[11];
+  const int ns = snapshot_sections(ctx, seq_begin, n_seqs, ptr, bytes);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* b = static_cast<uint8_t*>(buf);
+  size_t off = 0;
+  for (int i = 0; i < ns; ++i) {
+    if (bytes[i]) {
+      void* dst = out ? static_cast<void*>(b + off) : ptr[i];
+      const void* src = out ? ptr[i] : static_cast<const void*>(b + off);
+      st = cuda_ok(ctx, cudaMemcpyAsync(dst, src, bytes[i], cudaMemcpyDefault, cs), out ? "export scores" : "import scores");
+      if (st != KVS_OK) return st;
+    }
+    off += round256(bytes[i]);
+  }
+  return KVS_OK;
 }
 
 }  // namespace
@@ -301,6 +361,12 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.e_blk = reinterpret_cast<double*>(w + p.e_blk);
   d.s_blk = reinterpret_cast<double*>(w + p.s_blk);
   d.t_blk = reinterpret_cast<double*>(w + p.t_blk);
+  d.traj = reinterpret_cast<float*>(w + p.traj);
+  d.traj_len = cfg->traj_len;
+  d.prof = reinterpret_cast<double*>(w + p.prof);
+  d.n_prof = 0;
+  for (int l = 0; l < cfg->num_layers && l < 32; ++l)
+    if (cfg->profile_layers >> l & 1u) d.prof_layer[d.n_prof++] = l;
   d.last_blk = reinterpret_cast<int32_t*>(w + p.last_blk);
   d.steps = reinterpret_cast<int32_t*>(w + p.steps);
   d.acc_tickets = reinterpret_cast<int32_t*>(w + p.acc_tickets);
@@ -615,6 +681,41 @@ kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs
   return KVS_OK;
 }
 
+kvs_status kvs_filter_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, int32_t score_kind, double theta,
+                             int32_t* d_ids, int32_t capacity, int32_t* d_count, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
+  if (theta != theta) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "theta is NaN");
+  if (!d_ids || !d_count || capacity < 1)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "output buffers missing or capacity < 1");
+  return cuda_ok(ctx, launch_filter(ctx->dev, seq_begin, n_seqs, score_kind, theta, d_ids, capacity, d_count,
+                                    reinterpret_cast<cudaStream_t>(stream)),
+                 "filter");
+}
+
+size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs) {
+  if (!ctx || n_seqs < 0 || n_seqs > ctx->cfg.max_seqs) return 0;
+  void* ptr[11];
+  size_t bytes[11];
+  const int ns = snapshot_sections(ctx, 0, n_seqs, ptr, bytes);
+  size_t total = 0;
+  for (int i = 0; i < ns; ++i) total += round256(bytes[i]);
+  return total;
+}
+
+kvs_status kvs_export_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* dst, size_t dst_bytes,
+                             kvs_stream_t stream) {
+  return snapshot_copy(ctx, seq_begin, n_seqs, dst, dst_bytes, true, stream);
+}
+
+kvs_status kvs_import_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const void* src, size_t src_bytes,
+                             kvs_stream_t stream) {
+  return snapshot_copy(ctx, seq_begin, n_seqs, const_cast<void*>(src), src_bytes, false, stream);
+}
+
 size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
   if (!ctx) return 0;
   const size_t slots = (size_t)ctx->plan.num_pages * kBlock, B = ctx->cfg.max_seqs, MB = ctx->plan.max_blocks;
@@ -629,6 +730,8 @@ size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
     case KVS_STATE_C_BLOCK: case KVS_STATE_E_BLOCK: case KVS_STATE_S_BLOCK: case KVS_STATE_T_BLOCK: return B * MB * 8;
     case KVS_STATE_STEPS: return B * 4;
     case KVS_STATE_BLOCK_TABLE: return B * MB * 4;
+    case KVS_STATE_TRAJECTORY: return B * MB * (size_t)ctx->cfg.traj_len * 4;
+    case KVS_STATE_LAYER_PROFILE: return B * MB * (size_t)ctx->dev.n_prof * 8;
     default: return 0;
   }
 }
@@ -658,6 +761,9 @@ kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst
     case KVS_STATE_S_BLOCK: src = d.s_blk; break;
     case KVS_STATE_STEPS: src = d.steps; break;
     case KVS_STATE_BLOCK_TABLE: src = d.block_table; break;
+    case KVS_STATE_LAYER_PROFILE: src = d.prof; break;
+    case KVS_STATE_TRAJECTORY:
+      return cuda_ok(ctx, launch_read_trajectory(d, static_cast<float*>(d_dst), cs), "read trajectory");
     case KVS_STATE_E_TOKEN: case KVS_STATE_E_BLOCK: case KVS_STATE_T_BLOCK:
       return cuda_ok(ctx, launch_read_ema(d, what, static_cast<double*>(d_dst), cs), "read score");
     default: return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "state item %d", what);

@@ -14,6 +14,8 @@
 //     resident count [max_seqs]; free page stack [num_pages] + top
 //     score tables C/E per token [max_seqs][max_positions] double, stamp int32;
 //     C/E per block [max_seqs][max_blocks] double, stamp int32; steps [max_seqs] int32
+//     side-car: trajectory ring [max_seqs][max_blocks][traj_len] float, layer profiles
+//     [max_seqs][max_blocks][profiled layers] double
 //     attend partials: output rows [(grid_max + max_seqs)][Hq][D] float and (m, l) words
 //     [(grid_max + max_seqs)][Hq] u64; arrival counters
 //     logit scratch (the general kernel, and the tensor kernel when logits do not fit
@@ -80,6 +82,9 @@ struct Dev {
   double* c_tok; double* e_tok; int32_t* last_tok;   // [max_seqs][max_positions]
   double* c_blk; double* e_blk; int32_t* last_blk;   // [max_seqs][max_blocks]
   double* s_blk; double* t_blk;                      // [max_seqs][max_blocks] summed over entries
+  float* traj;  int32_t traj_len;                    // [max_seqs][max_blocks][traj_len] ring of t_blk
+  double* prof; int32_t n_prof;                      // [max_seqs][max_blocks][n_prof] layer profiles
+  int32_t prof_layer[4];                             // profiled layers, ascending
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
   float* partials;        // [records][Hq][D] partial output rows, records = kGridMax + max_seqs
@@ -187,6 +192,9 @@ cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
                           int32_t* keep_count, cudaStream_t st);
 cudaError_t launch_read_ema(const Dev& d, int what, double* dst, cudaStream_t st);
+cudaError_t launch_read_trajectory(const Dev& d, float* dst, cudaStream_t st);
+cudaError_t launch_filter(const Dev& d, int seq_begin, int n_seqs, int score_kind, double theta, int32_t* ids,
+                          int capacity, int32_t* count, cudaStream_t st);
 cudaError_t launch_clear(const Dev& d, cudaStream_t st);
 size_t general_smem_bytes(int Hq, int D);
 }  // namespace kvs

@@ -52,7 +52,9 @@ __device__ __forceinline__ double block_entry_sum(double x) {
 
 // Block k of sequence s at step `step`, whose entries' scores sum to xsum; returns the
 // new cumulative score in *c_new and the new EMA in *e_new.  The token-sum score
-// (H2O) accumulates xsum, and the TOVA score is xsum.
+// (H2O) accumulates xsum, and the TOVA score is xsum.  Side-car views ("Context views
+// at marginal cost", Tier 1): the trajectory ring keeps xsum in slot step % traj_len,
+// and each profiled layer's sum gains that layer's block mass.
 __device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int32_t step, double xsum,
                                              double* c_new, double* e_new) {
   float y = 0.f;
@@ -67,6 +69,9 @@ __device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int
   d.e_blk[t] = e;
   d.s_blk[t] += xsum;
   d.t_blk[t] = xsum;
+  if (d.traj_len) d.traj[t * d.traj_len + step % d.traj_len] = (float)xsum;
+  for (int i = 0; i < d.n_prof; ++i)
+    d.prof[t * d.n_prof + i] += (double)d.blk_mass[(size_t)d.prof_layer[i] * d.blk_layer_elems + t];
   d.last_blk[t] = step;
   *c_new = c;
   *e_new = e;

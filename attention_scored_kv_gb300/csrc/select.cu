@@ -176,7 +176,43 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
   }
 }
 
+// Threshold view ("Context views at marginal cost", Tier 1: a view filters the kept
+// table by a_s > theta): one CTA per sequence writes the resident blocks whose score
+// exceeds theta, in ascending id, 512 candidates per pass.
+__global__ void __launch_bounds__(kThreads) filter_kernel(Dev d, int seq_begin, int kind, double theta,
+                                                            int32_t* ids, int capacity, int32_t* count) {
+  __shared__ SelShared sh;
+  const int sl = blockIdx.x, s = seq_begin + sl, tid = threadIdx.x;
+  const SeqBlocks sb = seq_blocks(d, 0, s);
+  const int32_t steps_now = d.steps[s];
+  int before = 0;
+  for (int base = 0; base < sb.n; base += kThreads) {
+    const int i = base + tid;
+    int32_t k = -1;
+    int pass = 0;
+    if (i < sb.n) {
+      int32_t page;
+      k = block_at(d, s, sb, i, &page);
+      pass = block_score<false>(d, s, k, kind, steps_now) > theta;
+    }
+    int total;
+    const int out = before + block_scan(pass, sh, &total);
+    if (pass) {
+      if (out < capacity) ids[(size_t)sl * capacity + out] = k;
+      else set_error(d, kErrCapacity);
+    }
+    before += total;
+  }
+  if (tid == 0) count[sl] = before;
+}
+
 }  // namespace
+
+cudaError_t launch_filter(const Dev& d, int seq_begin, int n_seqs, int score_kind, double theta, int32_t* ids,
+                          int capacity, int32_t* count, cudaStream_t st) {
+  filter_kernel<<<n_seqs, kThreads, 0, st>>>(d, seq_begin, score_kind, theta, ids, capacity, count);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,

@@ -23,16 +23,12 @@ __device__ __forceinline__ bool protected_block(const Dev& d, int32_t k, int64_t
   return b0 < d.h2o_sink_tokens || b1 > next - d.h2o_recent_tokens;
 }
 
-// Key of the i-th resident block of sequence s (its id and page to *kid, *page): the
-// cumulative score, the EMA as of step steps_now - 1, the token sum, or the TOVA score
-// of step steps_now - 1 (0 for a block that step did not update); ~0 when protected.
-// L2ONLY reads the tables through L2 only (they were just written by other CTAs).
+// Score of block k of sequence s (a kvs_score_kind): the cumulative score, the EMA as
+// of step steps_now - 1, the token sum, or the TOVA score of step steps_now - 1 (0 for
+// a block that step did not update).  L2ONLY reads the tables through L2 only (they
+// were just written by other CTAs).
 template <bool L2ONLY>
-__device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlocks& sb, int i, int kind, bool protect,
-                                             int32_t steps_now, int32_t* kid, int32_t* page) {
-  const int32_t k = block_at(d, s, sb, i, page);
-  *kid = k;
-  if (protect && protected_block(d, k, sb.next)) return ~0ull;
+__device__ __forceinline__ double block_score(const Dev& d, int s, int32_t k, int kind, int32_t steps_now) {
   const size_t t = (size_t)s * d.max_blocks + k;
   double v;
   if (kind == KVS_SCORE_CUMULATIVE) {
@@ -49,7 +45,18 @@ __device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlock
     const int32_t gap = steps_now - 1 - last;
     v = (last < 0) ? 0.0 : (gap == 0 ? e : e * pow(d.ema_decay, (double)gap));
   }
-  return order_key(v);
+  return v;
+}
+
+// Key of the i-th resident block of sequence s (its id and page to *kid, *page): the
+// order key of its block_score, ~0 when protected.
+template <bool L2ONLY>
+__device__ __forceinline__ uint64_t cand_key(const Dev& d, int s, const SeqBlocks& sb, int i, int kind, bool protect,
+                                             int32_t steps_now, int32_t* kid, int32_t* page) {
+  const int32_t k = block_at(d, s, sb, i, page);
+  *kid = k;
+  if (protect && protected_block(d, k, sb.next)) return ~0ull;
+  return order_key(block_score<L2ONLY>(d, s, k, kind, steps_now));
 }
 
 }  // namespace kvs

@@ -39,6 +39,10 @@ __global__ void reset_kernel(Dev d, int seq_begin) {
     d.t_blk[blk_base + k] = 0.0;
     d.last_blk[blk_base + k] = -1;
   }
+  for (size_t i = threadIdx.x; i < (size_t)d.max_blocks * d.traj_len; i += blockDim.x)
+    d.traj[blk_base * d.traj_len + i] = 0.f;
+  for (size_t i = threadIdx.x; i < (size_t)d.max_blocks * d.n_prof; i += blockDim.x)
+    d.prof[blk_base * d.n_prof + i] = 0.0;
   if (d.mode == KVS_MODE_H2O) {
     // return every page of the sequence to the pool and clear its slots
     const int n = d.res_count[s];
@@ -86,6 +90,22 @@ __global__ void read_ema_kernel(const double* e, const int32_t* last, const int3
   }
 }
 
+// Trajectory ring, oldest step first: column j of block k is step tau = steps - T + j,
+// kept where the block was updated at tau.  A block is updated at every step of one
+// stretch of residency (it never returns once it leaves), so its slot tau % T holds
+// step tau exactly when 0 <= tau <= last; otherwise the column is 0.
+__global__ void read_trajectory_kernel(Dev d, float* dst) {
+  const int T = d.traj_len;
+  const size_t n = (size_t)d.max_seqs * d.max_blocks * T;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t kb = i / T;                 // s * max_blocks + k
+    const int j = (int)(i % T);
+    const int s = (int)(kb / d.max_blocks);
+    const int32_t tau = d.steps[s] - T + j, last = d.last_blk[kb];
+    dst[i] = (tau >= 0 && tau <= last) ? d.traj[kb * T + tau % T] : 0.f;
+  }
+}
+
 int grid_for(size_t n) {
   size_t g = (n + 255) / 256;
   if (g > 4096) g = 4096;
@@ -109,6 +129,12 @@ cudaError_t launch_init(const Dev& d, cudaStream_t st) {
 
 cudaError_t launch_reset(const Dev& d, int seq_begin, int n_seqs, cudaStream_t st) {
   reset_kernel<<<n_seqs, 256, 0, st>>>(d, seq_begin);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_read_trajectory(const Dev& d, float* dst, cudaStream_t st) {
+  const size_t n = (size_t)d.max_seqs * d.max_blocks * d.traj_len;
+  read_trajectory_kernel<<<grid_for(n), 256, 0, st>>>(d, dst);
   return cudaGetLastError();
 }
 

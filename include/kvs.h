@@ -119,7 +119,11 @@ typedef struct {
                                 (a CTA that is not the last to arrive reports KVS_ERR_TIMEOUT) */
   int32_t kv_dtype;          /* storage: KVS_F32, KVS_BF16 or KVS_E4M3 */
   int32_t in_dtype;          /* dtype of Q, K, V inputs: KVS_F32 or KVS_BF16 */
-  int32_t reserved_i[5];     /* must be 0 */
+  int32_t traj_len;          /* side-car trajectory ring: the last N steps' TOVA block score
+                                per block (0 = off, at most 256) */
+  uint32_t profile_layers;   /* side-car layer profiles: bit l set = keep, per block, the
+                                sum over steps of layer l's block mass (at most 4 bits) */
+  int32_t reserved_i[3];     /* must be 0 */
   double  h2o_recent_frac;   /* H2O: always keep the last frac * budget tokens (0.25) */
   double  ema_decay;         /* d in E <- d*E + (1-d)*x, in [0, 1) (0.9) */
   double  reserved_d[2];     /* must be 0 */
@@ -284,6 +288,35 @@ KVS_API kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_
                                  uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                                  int32_t* d_keep_count, kvs_stream_t stream);
 
+/* Threshold view ("Context views at marginal cost", Tier 1: a view is a filter of the
+ * kept score table, a_s > theta): per sequence of the range, the resident blocks whose
+ * block score (a kvs_score_kind, read as kvs_select_blocks reads it) is strictly
+ * greater than theta, in ascending id.  d_ids: [n_seqs][capacity] int32 (device);
+ * d_count: [n_seqs] int32 (device), the number that passed (ids beyond capacity are
+ * dropped and flag KVS_ERR_CAPACITY on the device).  Reads the tables only.
+ * Errors: KVS_ERR_INVALID_ARGUMENT for an unknown score kind, a NaN theta or missing
+ * buffers. */
+KVS_API kvs_status kvs_filter_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, int32_t score_kind,
+                                     double theta, int32_t* d_ids, int32_t capacity, int32_t* d_count,
+                                     kvs_stream_t stream);
+
+/* Score snapshot (the side-car kept next to the session's KV: "Context views at
+ * marginal cost", Tier 1).  Export copies, for the sequences of the range, every score
+ * table (token and block cumulative, EMA and update stamps, token-sum and TOVA block
+ * scores, the trajectory ring, the layer profiles) and the step counts into one
+ * buffer; import copies such a buffer back into a range of the same length.  The
+ * buffer is raw and carries no header: it can be imported only into a context created
+ * with the same max_positions, traj_len and profile_layers (the KV entries and the
+ * residency are not part of it).  The buffer may be device memory or host memory
+ * (pinned memory keeps the copies asynchronous); it must hold
+ * kvs_scores_snapshot_bytes(ctx, n_seqs) bytes.  One cudaMemcpyAsync per table on
+ * `stream`.  Errors: KVS_ERR_CAPACITY for a short buffer. */
+KVS_API size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs);
+KVS_API kvs_status kvs_export_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* dst, size_t dst_bytes,
+                                     kvs_stream_t stream);
+KVS_API kvs_status kvs_import_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const void* src,
+                                     size_t src_bytes, kvs_stream_t stream);
+
 /* State read-back (tests, inspection).  Copies one array of `layer` (ignored for
  * per-sequence items) into d_dst (device), which must hold kvs_state_bytes(). */
 typedef enum {
@@ -303,7 +336,10 @@ typedef enum {
   KVS_STATE_BLOCK_TABLE = 13,/* [max_seqs][max_blocks] int32 page of each block, -1 = none */
   KVS_STATE_S_BLOCK = 14,    /* [max_seqs][max_blocks] float64 TOKEN_SUM block score */
   KVS_STATE_T_BLOCK = 15,    /* [max_seqs][max_blocks] float64 TOVA block score of the last step */
-  KVS_STATE_COUNT = 16
+  KVS_STATE_TRAJECTORY = 16, /* [max_seqs][max_blocks][traj_len] float32, oldest step first,
+                                0 where the block was not updated (traj_len > 0) */
+  KVS_STATE_LAYER_PROFILE = 17, /* [max_seqs][max_blocks][profiled layers, ascending] float64 */
+  KVS_STATE_COUNT = 18
 } kvs_state_item;
 
 KVS_API size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what);

@@ -18,8 +18,9 @@ SCORE_TOL = 1e-4                                       # absolute, masses and sc
 _FMT = {"f32": kvs.F32, "bf16": kvs.BF16, "e4m3": kvs.E4M3}
 
 
-def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0):
+def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_layers=()):
     return kvs.config_init(
+        traj_len=traj_len, profile_layers=sum(1 << l for l in profile_layers),
         num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
         max_seqs=wl.batch, max_positions=wl.max_positions, window=wl.window, block_tokens=wl.block_tokens,
         h2o_budget_tokens=wl.h2o_budget_tokens, h2o_sink_tokens=wl.h2o_sink_tokens,
@@ -27,8 +28,8 @@ def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0):
         in_dtype=_FMT[wl.in_dtype], kernel=kernel, spin_limit=spin_limit)
 
 
-def make_oracle(wl, n):
-    return OracleKV(num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+def make_oracle(wl, n, traj_len=0, profile_layers=()):
+    return OracleKV(traj_len=traj_len, profile_layers=tuple(profile_layers),num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
                     head_dim=wl.head_dim, num_seqs=n, max_positions=wl.max_positions, kv_format=wl.kv_format,
                     window=wl.window, h2o_budget_tokens=wl.h2o_budget_tokens,
                     h2o_sink_tokens=wl.h2o_sink_tokens, h2o_recent_frac=wl.h2o_recent_frac,
@@ -100,13 +101,14 @@ class StateView:
 class Run:
     """One workload on the GPU, with the oracle tracking ``oracle_seqs``."""
 
-    def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0, fused=False):
+    def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0, fused=False,
+                 traj_len=0, profile_layers=()):
         self.wl = wl
         self.fused = fused            # decode steps through append_attend (one call per layer)
         self.inp = workloads.Inputs(wl, device=device)
-        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit))
+        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit, traj_len, profile_layers))
         self.oseqs = list(oracle_seqs)
-        self.oracle = make_oracle(wl, len(self.oseqs)) if self.oseqs else None
+        self.oracle = make_oracle(wl, len(self.oseqs), traj_len, profile_layers) if self.oseqs else None
         self.lens = self.inp.prefill_lengths()
         self.step = 0
         self.last_out = {}

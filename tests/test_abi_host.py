@@ -61,12 +61,27 @@ def cfg35b(**kw):
     ("max_seqs", 0, _abi.ERR_INVALID_ARGUMENT),
     ("kv_dtype", 7, _abi.ERR_INVALID_ARGUMENT),
     ("in_dtype", _abi.E4M3, _abi.ERR_INVALID_ARGUMENT),
+    ("traj_len", -1, _abi.ERR_INVALID_ARGUMENT),
+    ("traj_len", 257, _abi.ERR_INVALID_ARGUMENT),
+    ("profile_layers", 1 << 10, _abi.ERR_INVALID_ARGUMENT),     # layer 10 of 10
+    ("profile_layers", 0b11111, _abi.ERR_INVALID_ARGUMENT),     # five layers
 ])
 def test_invalid_configs_rejected(field, value, status):
     cfg = cfg35b(**{field: value})
     st, msg = kvs.validate_config(cfg)
     assert st == status and msg
     assert kvs.workspace_bytes(cfg) == 0
+
+
+def test_sidecar_workspace():
+    """The trajectory ring (float32 per block and step) and the layer profiles (float64
+    per block and profiled layer) add their bytes to the workspace."""
+    base = kvs.workspace_bytes(cfg35b())
+    mb = -(-32896 // 16)
+    grown = kvs.workspace_bytes(cfg35b(traj_len=64, profile_layers=0b1001))
+    assert kvs.validate_config(cfg35b(traj_len=64, profile_layers=0b1001))[0] == _abi.OK
+    assert grown - base >= 16 * mb * (64 * 4 + 2 * 8)
+    assert grown - base <= 16 * mb * (64 * 4 + 2 * 8) + 2 * 256
 
 
 def test_reserved_fields_must_be_zero():
