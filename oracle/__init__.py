@@ -24,11 +24,13 @@ What it computes, each piece citing the page passage it follows:
                    bookkeeping against a full sliding-mask recompute.
 * ``selection``  - sort-based top-k with ties to the lower block id, and the H2O
                    protected regions.
+* ``snapkv``     - SnapKV prefill scoring: observation-window votes, max-pooled with
+                   kernel 7 ("Context views at marginal cost", per-system reductions).
 * ``memory``     - the KV memory arithmetic ("Context Optimization", Memory Budget
                    Calculator).
 
 Parity status per function is listed in each module header.
 """
 
-from . import e4m3, attention, selection, memory, slot_cache, cache  # noqa: F401
+from . import e4m3, attention, selection, memory, slot_cache, snapkv, cache  # noqa: F401
 from .cache import OracleKV  # noqa: F401

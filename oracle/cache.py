@@ -32,7 +32,7 @@ Everything is float64 and written out plainly; no blocking or reordering.
 
 import numpy as np
 
-from . import attention, e4m3, selection
+from . import attention, e4m3, selection, snapkv
 
 
 class ScoreTables:
@@ -233,6 +233,26 @@ class OracleKV:
         k, v = self.stored_kv(layer, seq, pos)
         out, w = attention.decode_attention(q, k, v)
         return out, w, pos
+
+    def prefill_score(self, layer, seq, q_obs, kernel=7):
+        """SnapKV prefill scoring (``oracle.snapkv``): the last n_obs prompt queries
+        q_obs [n_obs, Hq, D] (positions next_position - n_obs .. next_position - 1)
+        attend causally over the resident entries; the votes are max-pooled (kernel 7)
+        and recorded as this layer's step masses, as an attend records its weights.
+        Returns (votes [Hq, n], pooled [Hq, n], positions [n])."""
+        q_obs = np.asarray(q_obs, np.float64)
+        nxt = int(self.next_position[layer, seq])
+        n_obs = q_obs.shape[0]
+        if n_obs < 1 or n_obs > nxt or (self.mode == "window" and n_obs > self.window):
+            raise ValueError("the observation window must hold 1 .. min(prompt, window) queries")
+        pos = self.resident_positions(layer, seq)
+        k, _ = self.stored_kv(layer, seq, pos)
+        votes = snapkv.observation_votes(q_obs, np.arange(nxt - n_obs, nxt), k, pos)
+        pooled = snapkv.max_pool(votes, pos, kernel)
+        self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(pooled))
+        self._blk_mass[(layer, seq)] = attention.block_step_mass(pooled, pos, self.block)
+        self._attended.add((layer, seq))
+        return votes, pooled, pos
 
     def token_mass(self, layer, seq):
         """(positions, token mass) of the last attend of (layer, seq)."""
