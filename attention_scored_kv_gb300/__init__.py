@@ -185,6 +185,16 @@ class KVCache:
                                                            _stream(stream)))
         return out
 
+    def prefill_score(self, layer, q_obs, seq_begin=0, stream=None):
+        """SnapKV prefill scoring of one layer: q_obs [n_seqs, n_obs, Hq, D] bf16 CUDA
+        tensor, the queries of each prompt's last n_obs positions."""
+        if not isinstance(q_obs, torch.Tensor) or not q_obs.is_cuda or q_obs.dim() != 4:
+            raise TypeError("q_obs must be a 4-d CUDA tensor")
+        L, Hq, Hkv, D = self.shape
+        n, n_obs = q_obs.shape[0], q_obs.shape[1]
+        _need(q_obs, "q_obs", torch.bfloat16, (n, n_obs, Hq, D))
+        self._check(lib().kvs_prefill_score(self._ctx, layer, seq_begin, n, _ptr(q_obs), n_obs, _stream(stream)))
+
     def accumulate_scores(self, seq_begin=0, n_seqs=None, stream=None):
         n = self.cfg.max_seqs - seq_begin if n_seqs is None else n_seqs
         self._check(lib().kvs_accumulate_scores(self._ctx, seq_begin, n, _stream(stream)))

@@ -34,7 +34,8 @@ class Config(ctypes.Structure):
         ("window", ctypes.c_int32), ("block_tokens", ctypes.c_int32), ("h2o_budget_tokens", ctypes.c_int32),
         ("h2o_sink_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("spin_limit", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
-        ("traj_len", ctypes.c_int32), ("profile_layers", ctypes.c_uint32), ("reserved_i", ctypes.c_int32 * 3),
+        ("traj_len", ctypes.c_int32), ("profile_layers", ctypes.c_uint32), ("obs_window", ctypes.c_int32),
+        ("reserved_i", ctypes.c_int32 * 2),
         ("h2o_recent_frac", ctypes.c_double), ("ema_decay", ctypes.c_double),
         ("reserved_d", ctypes.c_double * 2),
     ]
@@ -61,6 +62,7 @@ _SIGS = {
     "kvs_attend_blocks": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
     "kvs_decode_attend_static_scratch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "kvs_accumulate_scores": (_I, [_P, _I, _I, _P]),
+    "kvs_prefill_score": (_I, [_P, _I, _I, _I, _P, _I, _P]),
     "kvs_select_blocks": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
     "kvs_accumulate_select": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
     "kvs_filter_blocks": (_I, [_P, _I, _I, _I, ctypes.c_double, _P, _I, _P, _P]),

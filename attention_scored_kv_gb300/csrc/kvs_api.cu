@@ -45,7 +45,8 @@ struct Plan {
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
   size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, traj, prof, steps, acc_tickets;
-  size_t partials, part_ml, counters, logits, err;
+  size_t partials, part_ml, counters, logits, ps_part, ps_stat, ps_tok, ps_blk, ps_tickets, err;
+  int ps_bound = 0, ps_chunks = 0;
 };
 
 size_t esize(int dt) { return dt == KVS_F32 ? 4 : (dt == KVS_BF16 ? 2 : 1); }
@@ -94,10 +95,19 @@ kvs_status check_config(const kvs_config* c, char* msg, size_t n) {
     put(msg, n, "profile_layers: at most 4 bits, each below num_layers");
     return KVS_ERR_INVALID_ARGUMENT;
   }
-  for (int i = 0; i < 3; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  for (int i = 0; i < 2; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->obs_window < 0 || c->obs_window > prefill_obs_max()) {
+    put(msg, n, "obs_window must be in [0, %d]", prefill_obs_max());
+    return KVS_ERR_INVALID_ARGUMENT;
+  }
   for (int i = 0; i < 2; ++i) if (c->reserved_d[i] != 0.0) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
   const int mode = c->h2o_budget_tokens > 0 ? KVS_MODE_H2O : (c->window > 0 ? KVS_MODE_WINDOW : KVS_MODE_NONE);
   const bool tc = tc_supported(c->num_q_heads, c->num_kv_heads, c->head_dim, c->kv_dtype, c->in_dtype, c->window, mode);
+  if (c->obs_window > 0 && !tc) {
+    put(msg, n, "SnapKV prefill scoring (obs_window > 0) needs the tensor-core configuration: head_dim 128, 8 query "
+                "heads per KV head, bf16 inputs, bf16 or E4M3 storage");
+    return KVS_ERR_UNSUPPORTED;
+  }
   if (c->kernel == KVS_KERNEL_TENSOR && !tc) {
     put(msg, n, "the tensor-core kernel needs head_dim 128, 8 query heads per KV head (4 or 8 KV heads), bf16 "
                 "inputs, bf16 or E4M3 storage and a window that is 0 or a multiple of 16");
@@ -168,6 +178,16 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->part_ml = take(((size_t)kGridMax + B) * Hq * 8);
   p->counters = take((size_t)kCounterInts * B * 4);
   p->logits = take(p->logit_elems * 4);
+  // prefill scoring scratch: chunks of at least kPrefillChunkMin resident blocks
+  const bool ps = c->obs_window > 0;
+  p->ps_bound = ps ? p->res_blocks_per_seq : 0;
+  p->ps_chunks = ps ? (int)cdiv64(p->ps_bound, kPrefillChunkMin) : 0;
+  const size_t Hkv = c->num_kv_heads;
+  p->ps_part = take(B * p->ps_chunks * Hq * 32 * 8);
+  p->ps_stat = take(ps ? B * Hq * 32 * 8 : 0);
+  p->ps_tok = take(B * Hkv * p->ps_bound * kBlock * 4);
+  p->ps_blk = take(B * Hkv * p->ps_bound * 4);
+  p->ps_tickets = take(B * p->ps_chunks * 4);
   p->err = take(4);
   p->total = o;
 }
@@ -376,6 +396,12 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.logit_scratch = reinterpret_cast<float*>(w + p.logits);
   d.logit_scratch_elems = p.logit_elems;
   d.err = reinterpret_cast<int32_t*>(w + p.err);
+  d.ps_part = reinterpret_cast<float2*>(w + p.ps_part);
+  d.ps_stat = reinterpret_cast<float2*>(w + p.ps_stat);
+  d.ps_tok = reinterpret_cast<float*>(w + p.ps_tok);
+  d.ps_blk = reinterpret_cast<float*>(w + p.ps_blk);
+  d.ps_tickets = reinterpret_cast<int32_t*>(w + p.ps_tickets);
+  d.ps_bound = p.ps_bound;
 
   const bool tc = tc_supported(cfg->num_q_heads, cfg->num_kv_heads, cfg->head_dim, cfg->kv_dtype, cfg->in_dtype,
                                cfg->window, p.mode);
@@ -562,6 +588,39 @@ kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
                                        n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
                                        reinterpret_cast<cudaStream_t>(stream)),
                  "tensor-core block-list attend");
+}
+
+kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_q_obs,
+                             int32_t n_obs, kvs_stream_t stream) {
+  if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
+  if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
+  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  if (st != KVS_OK) return st;
+  if (ctx->cfg.obs_window == 0)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "prefill scoring is off: create the context with obs_window > 0");
+  if (n_obs < 1 || n_obs > ctx->cfg.obs_window)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "n_obs must be in [1, obs_window = %d]", ctx->cfg.obs_window);
+  if (!d_q_obs || (reinterpret_cast<uintptr_t>(d_q_obs) & 15))
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q_obs must be a 16-byte aligned device pointer");
+  const int B = ctx->cfg.max_seqs;
+  int64_t maxb = 1;
+  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    const int64_t nx = ctx->next[(size_t)layer * B + s];
+    if (nx < n_obs)
+      return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence %d holds %lld entries in layer %d, fewer than n_obs", s,
+                  (long long)nx, layer);
+    if (ctx->plan.mode == KVS_MODE_WINDOW && n_obs > ctx->cfg.window)
+      return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "n_obs exceeds the window");
+    maxb = std::max(maxb, seq_block_bound(ctx, s));
+  }
+  maxb = std::min<int64_t>(maxb, ctx->plan.ps_bound);
+  // chunk size: about four CTAs per SM over the launch, 16..64 blocks each
+  const int64_t units = maxb * n_seqs * ctx->cfg.num_kv_heads, target = 4 * (int64_t)ctx->sm_count;
+  const int cb = (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, target)));
+  const int chunks = (int)cdiv64(maxb, cb);
+  return cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, seq_begin, n_seqs, d_q_obs, n_obs, cb, chunks,
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                 "prefill score");
 }
 
 kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,

@@ -32,6 +32,7 @@ namespace kvs {
 
 constexpr int kBlock = 16;          // tokens per block (placement unit)
 constexpr int kGridMax = 256;       // upper bound of persistent attend CTAs (sizing)
+constexpr int kPrefillChunkMin = 16, kPrefillChunkMax = 64;   // blocks per prefill-scoring CTA
 
 // Device error word bits.
 enum : int32_t {
@@ -85,6 +86,12 @@ struct Dev {
   float* traj;  int32_t traj_len;                    // [max_seqs][max_blocks][traj_len] ring of t_blk
   double* prof; int32_t n_prof;                      // [max_seqs][max_blocks][n_prof] layer profiles
   int32_t prof_layer[4];                             // profiled layers, ascending
+  // prefill scoring scratch (obs_window > 0): row partials [max_seqs][chunks][Hq][32] and
+  // statistics [max_seqs][Hq][32] as (max, sum) / (max, 1/sum); per KV head the entry
+  // sums [max_seqs][Hkv][ps_bound][16] and block values [max_seqs][Hkv][ps_bound];
+  // tickets [max_seqs][chunks]
+  float2* ps_part; float2* ps_stat; float* ps_tok; float* ps_blk; int32_t* ps_tickets;
+  int32_t ps_bound;
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
   float* partials;        // [records][Hq][D] partial output rows, records = kGridMax + max_seqs
@@ -196,5 +203,8 @@ cudaError_t launch_read_trajectory(const Dev& d, float* dst, cudaStream_t st);
 cudaError_t launch_filter(const Dev& d, int seq_begin, int n_seqs, int score_kind, double theta, int32_t* ids,
                           int capacity, int32_t* count, cudaStream_t st);
 cudaError_t launch_clear(const Dev& d, cudaStream_t st);
+int prefill_obs_max();
+cudaError_t launch_prefill_score(const Dev& d, int layer, int seq_begin, int n_seqs, const void* q_obs, int n_obs,
+                                 int chunk_blocks, int n_chunks, cudaStream_t st);
 size_t general_smem_bytes(int Hq, int D);
 }  // namespace kvs

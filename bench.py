@@ -190,7 +190,24 @@ def make_config(kvs, wl):
         max_seqs=wl.batch, max_positions=wl.max_positions, window=wl.window, block_tokens=wl.block_tokens,
         h2o_budget_tokens=wl.h2o_budget_tokens, h2o_sink_tokens=wl.h2o_sink_tokens,
         h2o_recent_frac=wl.h2o_recent_frac, ema_decay=wl.ema_decay, kv_dtype=fmt[wl.kv_format],
-        in_dtype=fmt[wl.in_dtype])
+        in_dtype=fmt[wl.in_dtype], obs_window=OBS_WINDOW if snapkv_capable(wl) else 0)
+
+
+OBS_WINDOW = 32      # SnapKV's observation window
+
+
+def snapkv_capable(wl):
+    """Prefill scoring runs on the tensor-core configurations."""
+    return wl.head_dim == 128 and wl.in_dtype == "bf16" and wl.num_q_heads == 8 * wl.num_kv_heads \
+        and wl.kv_format in ("bf16", "e4m3")
+
+
+def bf16_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
 
 
 def prefill(cache, inp, wl):
@@ -373,6 +390,34 @@ def run_ours(args, world, rank, local):
         reattend = {"blocks_kept": kept, "kv_bytes_per_launch": int(rbytes), "launch_us": round(reattend_us, 3),
                     "kv_gbs": round(rbytes / (reattend_us * 1e-6) / 1e9, 1),
                     "frac_of_hbm": round(rbytes / (reattend_us * 1e-6) / 1e9 / hbm, 4)}
+    # ---- SnapKV prefill scoring of every layer over the current cache (three launches
+    # per layer), graph of L layers; FLOPs = QK^T of the observation queries once
+    prefill_score = None
+    if cache.cfg.obs_window:
+        QO = torch.stack([inp.obs_q(l, OBS_WINDOW) for l in range(L)])
+        gp = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gp):
+            for l in range(L):
+                cache.prefill_score(l, QO[l])
+        for _ in range(2):
+            gp.replay()
+        torch.cuda.synchronize()
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        p0.record()
+        for _ in range(args.attend_reps):
+            gp.replay()
+        p1.record()
+        torch.cuda.synchronize()
+        assert cache.get_status() == 0, cache.last_error()
+        ps_us = p0.elapsed_time(p1) * 1e3 / (args.attend_reps * L)
+        qk_flops = 2.0 * OBS_WINDOW * Hq * entries * D
+        peak_tf, tf_kind = bf16_peak()
+        tf = qk_flops / (ps_us * 1e-6) / 1e12
+        prefill_score = {"n_obs": OBS_WINDOW, "layer_us": round(ps_us, 3), "launches_per_layer": 3,
+                         "qk_flops_per_layer": int(qk_flops), "tflops": round(tf, 1),
+                         "tflops_executed": round(2 * tf, 1), "peak_tflops": peak_tf, "peak_source": tf_kind,
+                         "frac": round(tf / peak_tf, 4), "frac_executed": round(2 * tf / peak_tf, 4),
+                         "k_bytes_per_layer_pass": int(entries * kv_bytes_per_entry(wl) // 2)}
     traffic = None                      # DRAM bytes per launch measured by ncu, this workload only
     if wl0.name == "e4m3-b16-ctx32768-window4096":
         traffic = profiled_traffic(["attention_scored_kv_gb300/csrc/attend_tc.cu",
@@ -447,6 +492,7 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": round(e2e_value, 2), "unit": "decode steps/s", "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps},
         "reattend": reattend,
+        "prefill_score": prefill_score,
         "gpu_launches": int(per_step_launches * args.steps),
         "clocks": clocks,
     }

@@ -123,7 +123,9 @@ typedef struct {
                                 per block (0 = off, at most 256) */
   uint32_t profile_layers;   /* side-car layer profiles: bit l set = keep, per block, the
                                 sum over steps of layer l's block mass (at most 4 bits) */
-  int32_t reserved_i[3];     /* must be 0 */
+  int32_t obs_window;        /* SnapKV prefill scoring: the most observation queries one
+                                kvs_prefill_score call takes (1..32); 0 = off */
+  int32_t reserved_i[2];     /* must be 0 */
   double  h2o_recent_frac;   /* H2O: always keep the last frac * budget tokens (0.25) */
   double  ema_decay;         /* d in E <- d*E + (1-d)*x, in [0, 1) (0.9) */
   double  reserved_d[2];     /* must be 0 */
@@ -245,6 +247,26 @@ KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_be
 KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
                                                     int32_t n_seqs, const void* d_q, float* d_out,
                                                     kvs_stream_t stream);
+
+/* SnapKV prefill scoring ("Context views at marginal cost", the per-system
+ * reductions: observation window of the prompt's last queries, votes pooled per token
+ * and head, max-pool kernel 7).  Call it for a layer once its prompt is appended, in
+ * place of the attend of a decode step; kvs_accumulate_scores after the last layer
+ * then folds the result into the tables as their first step.
+ * d_q_obs: [n_seqs][n_obs][num_q_heads][head_dim] bf16 (device, 16-byte aligned), the
+ * queries of the last n_obs positions of each sequence's prompt, oldest first.  Query
+ * i, at position next_position - n_obs + i, attends over the resident entries at
+ * positions <= its own: logits q.k/sqrt(D), softmax per head.  An entry's vote for
+ * head h sums the weights of the n_obs queries of head h.  The votes are max-pooled:
+ * at each resident position, the largest vote among the resident positions within 3
+ * of it.  The pooled votes replace the layer's step masses: the entry mass is their
+ * sum over heads, and the block mass the max over heads of the in-block sum.  E4M3
+ * caches round the queries to f16, as the decode attend does.
+ * Needs a context created with obs_window >= n_obs (tensor-core configurations
+ * only).  Errors: KVS_ERR_INVALID_ARGUMENT for n_obs outside [1, obs_window], a
+ * sequence holding fewer than n_obs entries, or (window mode) n_obs > window. */
+KVS_API kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
+                                     const void* d_q_obs, int32_t n_obs, kvs_stream_t stream);
 
 /* Fold this step's masses of every layer into the score tables of the range:
  * token score x_p = sum over layers of the entry masses, block score y_k = max over

@@ -18,9 +18,9 @@ SCORE_TOL = 1e-4                                       # absolute, masses and sc
 _FMT = {"f32": kvs.F32, "bf16": kvs.BF16, "e4m3": kvs.E4M3}
 
 
-def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_layers=()):
+def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_layers=(), obs_window=0):
     return kvs.config_init(
-        traj_len=traj_len, profile_layers=sum(1 << l for l in profile_layers),
+        obs_window=obs_window, traj_len=traj_len, profile_layers=sum(1 << l for l in profile_layers),
         num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
         max_seqs=wl.batch, max_positions=wl.max_positions, window=wl.window, block_tokens=wl.block_tokens,
         h2o_budget_tokens=wl.h2o_budget_tokens, h2o_sink_tokens=wl.h2o_sink_tokens,
@@ -102,11 +102,11 @@ class Run:
     """One workload on the GPU, with the oracle tracking ``oracle_seqs``."""
 
     def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0, fused=False,
-                 traj_len=0, profile_layers=()):
+                 traj_len=0, profile_layers=(), obs_window=0):
         self.wl = wl
         self.fused = fused            # decode steps through append_attend (one call per layer)
         self.inp = workloads.Inputs(wl, device=device)
-        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit, traj_len, profile_layers))
+        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit, traj_len, profile_layers, obs_window))
         self.oseqs = list(oracle_seqs)
         self.oracle = make_oracle(wl, len(self.oseqs), traj_len, profile_layers) if self.oseqs else None
         self.lens = self.inp.prefill_lengths()
@@ -138,6 +138,21 @@ class Run:
                                     seq_begin=s)
                     if s in self.oseqs:
                         self._oracle_append_chunks(l, self.oseqs.index(s), k, v, chunk)
+
+    def prefill_score(self, n_obs):
+        """SnapKV scoring of every layer on both sides, then the accumulate (the tables'
+        first step); returns the worst block- and entry-mass errors of the oracle's
+        sequences, read before the accumulate."""
+        wl, c = self.wl, self.cache
+        qs = [self.inp.obs_q(l, n_obs) for l in range(wl.num_layers)]
+        for l in range(wl.num_layers):
+            c.prefill_score(l, qs[l])
+            for i, s in enumerate(self.oseqs):
+                self.oracle.prefill_score(l, i, workloads.as_f64(qs[l][s]))
+        worst = check_masses(self)
+        c.accumulate_scores()
+        self.oracle.accumulate()
+        return worst
 
     def _oracle_append_chunks(self, l, i, k, v, chunk):
         kf, vf = workloads.as_f64(k), workloads.as_f64(v)

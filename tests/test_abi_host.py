@@ -86,7 +86,7 @@ def test_sidecar_workspace():
 
 def test_reserved_fields_must_be_zero():
     cfg = cfg35b()
-    cfg.reserved_i[2] = 1
+    cfg.reserved_i[1] = 1
     assert kvs.validate_config(cfg)[0] == _abi.ERR_INVALID_ARGUMENT
 
 

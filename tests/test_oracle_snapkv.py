@@ -137,3 +137,31 @@ def test_feeds_the_score_tables_as_a_first_step():
         sel = slice(16 * b, min(16 * b + 16, 50))
         y = max(np.max(pooled[l][:, sel].sum(axis=1)) for l in range(2))
         assert abs(sc.c_blk[b] - y) < 1e-12
+
+
+def test_planted_workload_keeps_the_fact_and_its_left_neighbour():
+    """"Per-Head Attention as a Scoring Signal", Example: on a scaled-down copy of the
+    planted workload (8192-token prompt, retrieval key at 4096, the first entry of
+    block 256), SnapKV scoring alone ranks the anchor, the fact and the recent blocks
+    into the kept set.  The pool carries the fact's vote to positions 4093..4095, so
+    block 255 is kept as well."""
+    import workloads
+    wl = workloads.scaled_down("bf16-b1-ctx131072-planted", context=8192, retrieval_pos=4096,
+                               num_layers=2, steps=1, prefill_chunk=0)
+    inp = workloads.Inputs(wl, device="cpu")
+    o = OracleKV(num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+                 head_dim=wl.head_dim, num_seqs=1, max_positions=wl.max_positions, kv_format="bf16")
+    fact_head = 2 * wl.group                       # KV head 2 carries the retrieval key
+    for l in range(wl.num_layers):
+        k, v = inp.prefill_kv(l, 0)
+        o.append(l, 0, workloads.as_f64(k), workloads.as_f64(v))
+        votes, pooled, pos = o.prefill_score(l, 0, workloads.as_f64(inp.obs_q(l, 32)[0]))
+        f = wl.retrieval_pos
+        assert np.argmax(votes[fact_head]) == f
+        assert np.all(pooled[fact_head, f - 3: f + 4] == votes[fact_head, f])
+    o.accumulate()
+    keep = set(o.select(0, wl.keep_k(len(o.resident_block_ids(0)))))
+    anchor = {p // 16 for p in range(51)}
+    recent = {p // 16 for p in range(wl.context - 100, wl.context)}
+    assert anchor <= keep and recent <= keep
+    assert {255, 256} <= keep

@@ -110,7 +110,7 @@ def scaled_down(base_name, **changes):
 
 # --------------------------------------------------------------------------- seeds
 _TAGS = {"q": 1, "k": 2, "v": 3, "pk": 4, "pv": 5, "heavy_p": 6, "heavy_s": 7,
-         "lengths": 8, "planted_u": 9}
+         "lengths": 8, "planted_u": 9, "oq": 10}
 
 
 def _splitmix64(x):
@@ -226,6 +226,17 @@ class Inputs:
             for kvh in range(min(4, wl.num_kv_heads)):
                 u = self._planted_u(layer, kvh)
                 q[:, kvh * wl.group, :] = math.sqrt(wl.head_dim) * u
+        return q.to(self.dtype)
+
+    def obs_q(self, layer, n_obs):
+        """Queries of the last n_obs prefill positions in one layer (SnapKV's observation
+        window): [B, n_obs, Hq, D], oldest first; planted heads as in step_q."""
+        wl = self.wl
+        q = self._randn((wl.batch, n_obs, wl.num_q_heads, wl.head_dim), "oq", layer)
+        if wl.planted:
+            for kvh in range(min(4, wl.num_kv_heads)):
+                u = self._planted_u(layer, kvh)
+                q[:, :, kvh * wl.group, :] = math.sqrt(wl.head_dim) * u
         return q.to(self.dtype)
 
     def step_kv(self, layer, step):
