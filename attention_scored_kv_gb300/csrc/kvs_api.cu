@@ -614,9 +614,12 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
     maxb = std::max(maxb, seq_block_bound(ctx, s));
   }
   maxb = std::min<int64_t>(maxb, ctx->plan.ps_bound);
-  // chunk size: about four CTAs per SM over the launch, 16..64 blocks each
-  const int64_t units = maxb * n_seqs * ctx->cfg.num_kv_heads, target = 4 * (int64_t)ctx->sm_count;
-  const int cb = (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, target)));
+  // chunk size: the largest (fewest CTAs, least fixed cost per block) unless the launch
+  // would then leave SMs idle: two CTAs fit an SM
+  const int64_t units = maxb * n_seqs * ctx->cfg.num_kv_heads, slots = 2 * (int64_t)ctx->sm_count;
+  const int cb = units >= (int64_t)kPrefillChunkMax * slots
+                     ? kPrefillChunkMax
+                     : (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, slots)));
   const int chunks = (int)cdiv64(maxb, cb);
   return cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, seq_begin, n_seqs, d_q_obs, n_obs, cb, chunks,
                                            reinterpret_cast<cudaStream_t>(stream)),

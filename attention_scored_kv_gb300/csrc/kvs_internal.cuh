@@ -32,7 +32,7 @@ namespace kvs {
 
 constexpr int kBlock = 16;          // tokens per block (placement unit)
 constexpr int kGridMax = 256;       // upper bound of persistent attend CTAs (sizing)
-constexpr int kPrefillChunkMin = 16, kPrefillChunkMax = 64;   // blocks per prefill-scoring CTA
+constexpr int kPrefillChunkMin = 16, kPrefillChunkMax = 32;   // blocks per prefill-scoring CTA
 
 // Device error word bits.
 enum : int32_t {
