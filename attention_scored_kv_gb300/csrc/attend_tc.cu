@@ -50,7 +50,15 @@ constexpr int kNCW = 8;                 // consumer warps
 // A ring stage: every stage completion costs a few hundred ns of barrier traffic, so
 // stages are large (48 KB: 6 E4M3 or 3 bf16 blocks of 4 KV heads); two or more stages.
 constexpr int kStageBytes = 48 * 1024;
-constexpr int kThreads = (kNCW + 1) * 32;
+constexpr int kProducer = kNCW;         // warp that issues the copies
+constexpr int kNormWarp = kNCW + 1;     // warp that combines the normaliser (whole plan)
+constexpr int kThreads = (kNCW + 2) * 32;
+// Named barriers: 1 all consumers, 2 + h the two consumer warps of KV head h, and in the
+// whole plan: consumers -> normaliser warp for the statistics words (kBarMl) and for
+// the partial output rows (kBarOut, producer warp), output warps among themselves
+// (kBarOutWarps).
+constexpr int kBarOut = 13, kBarMl = 14, kBarOutWarps = 15;
+constexpr int kPubThreads = (kNCW + 1) * 32;   // consumers arrive, one publishing warp waits
 constexpr int kMbarLimit = 1 << 22;     // polls of an mbarrier before giving up
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kVFold = 256.0f;        // E4M3: p * v_scale * 256 keeps P off f16 subnormals
@@ -99,6 +107,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
 }
+#ifndef KVS_VPREFETCH
+#define KVS_VPREFETCH 0
+#endif
+// L2 prefetches: hints only, nothing lands in shared memory and nothing completes on a
+// barrier.  The tensor form is bounds-checked against the map like a load.
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
+               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
                :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
@@ -110,6 +130,24 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ void named_sync(int id, int n) {
   __syncwarp();
   asm volatile("barrier.sync %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+// Named barrier that also returns the AND of every participant's v.
+__device__ __forceinline__ bool named_sync_and(int id, int n, bool v) {
+  __syncwarp();
+  uint32_t r;
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+               : "=r"(r) : "r"((uint32_t)v), "r"(id), "r"(n) : "memory");
+  return r != 0;
+}
+// Arrive on a named barrier of n threads without waiting (the waiters use named_sync).
+__device__ __forceinline__ void named_arrive(int id, int n) {
+  __syncwarp();
+  asm volatile("barrier.arrive %0, %1;" :: "r"(id), "r"(n) : "memory");
+}
+// Add with release semantics: what this thread wrote or saw before is visible GPU-wide
+// to whoever acquires the new value.
+__device__ __forceinline__ void red_release_add(int32_t* p, int32_t v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
 }
 __device__ __forceinline__ void red_add(int32_t* p, int32_t v) {
   asm volatile("red.relaxed.gpu.global.add.s32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
@@ -254,30 +292,22 @@ __device__ __forceinline__ void qk_blocks(const uint8_t* stage, const float* ssc
 // back over the logits, per-head in-block sums to bsum, the running l, and the MMAs
 // into the shared accumulators o (dimensions on M, heads on N).
 template <int HKV, bool FP8, int NB>
-__device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* sscale_st, int j0, int i_first, float* lg,
-                                          float* bsum, int kvh, int lane, float mh, float& lsum, float (&o)[8][4]) {
+__device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* sscale_st, int j0, int i_first,
+                                          const float* lg, int kvh, int lane, float (&o)[8][4]) {
   using C = Cfg<HKV, FP8>;
   constexpr int HQ = C::HQ, WPK = C::WPK;
   const int g = lane >> 2, t = lane & 3;
   const int hg = kvh * kG + g;
-  float p[NB][4];
+  float p[NB][4];                                       // weights exp2(s - m), from the sweep
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const int i = i_first + b * WPK;
-    float2* pa = reinterpret_cast<float2*>(lg + lidx<HQ>(i, hg, 2 * t));
-    float2* pb = reinterpret_cast<float2*>(lg + lidx<HQ>(i, hg, 2 * t + 8));
-    const float2 sa = *pa, sbv = *pb;
-    p[b][0] = exp2f(sa.x - mh);
-    p[b][1] = exp2f(sa.y - mh);
-    p[b][2] = exp2f(sbv.x - mh);
-    p[b][3] = exp2f(sbv.y - mh);
-    float bpart = (p[b][0] + p[b][1]) + (p[b][2] + p[b][3]);   // this thread's share of the block
-    lsum += bpart;
-    *pa = make_float2(p[b][0], p[b][1]);
-    *pb = make_float2(p[b][2], p[b][3]);
-    bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
-    bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-    if (t == 0) bsum[i * (HQ + 1) + hg] = bpart;        // rows padded by one float
+    const float2 pa = *reinterpret_cast<const float2*>(lg + lidx<HQ>(i, hg, 2 * t));
+    const float2 pb = *reinterpret_cast<const float2*>(lg + lidx<HQ>(i, hg, 2 * t + 8));
+    p[b][0] = pa.x;
+    p[b][1] = pa.y;
+    p[b][2] = pb.x;
+    p[b][3] = pb.y;
   }
   if constexpr (FP8) {
     uint32_t b0[NB], b1[NB];
@@ -335,8 +365,42 @@ __device__ __forceinline__ void pv_blocks(const uint8_t* stage, const float* ssc
   }
 }
 
+// Between the passes: every logit of the CTA's blocks [i0, i1) becomes its weight
+// p = exp2(s - m_h) in place (masked logits are -inf and give 0), each (block, head)
+// row's sum goes to bsum, and each thread's sum over its rows to lred.  Thread tid
+// keeps head tid % HQ, so the HQ-strided partials of lred add up to the head's l.
+template <int HQ>
+__device__ __forceinline__ void weights_sweep(float* lg, float* bsum, float* lred, const float* mseg, int i0,
+                                              int i1, int tid) {
+  constexpr int NT = kNCW * 32;
+  static_assert(NT % HQ == 0, "a thread keeps one head");
+  const int h = tid % HQ;
+  const float m = mseg[h];
+  float l = 0.f;
+  for (int i = i0 + tid / HQ; i < i1; i += NT / HQ) {
+    float4* row = reinterpret_cast<float4*>(lg + (size_t)i * lg_block<HQ>() + h * kBlock);
+    // chunk u ^ (h >> 1): the lanes of a quarter-warp then read eight different bank groups
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = row[(u ^ (h >> 1)) & 3];
+    float rs = 0.f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u].x = exp2f(v[u].x - m);
+      v[u].y = exp2f(v[u].y - m);
+      v[u].z = exp2f(v[u].z - m);
+      v[u].w = exp2f(v[u].w - m);
+      rs += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+      row[(u ^ (h >> 1)) & 3] = v[u];
+    }
+    bsum[i * (HQ + 1) + h] = rs;                      // rows padded by one float
+    l += rs;
+  }
+  lred[tid] = l;
+}
+
 constexpr int kSC = 32;                 // partial records per round of the normaliser
-constexpr int kRingBytes = 128 * 1024;  // shared memory given to the TMA ring at most
+constexpr int kRingBytes = 144 * 1024;  // shared memory given to the TMA ring at most
 constexpr int kMinStages = 2;
 
 struct Params {
@@ -382,12 +446,15 @@ __device__ __forceinline__ int32_t list_block(const Dev& d, int s, int32_t* k) {
 // Shared-memory carve-up (byte offsets from a 1024-aligned base); the ring comes first
 // so every stage keeps the 1024-byte alignment the 128-byte swizzle needs.
 struct SmemPlan {
-  size_t ring, sscale, bars, seqb, blk, prefix, mbuf, lbuf, hv, flag, pm, pl, bsum, obuf, lg, total;
+  size_t ring, sscale, bars, seqb, blk, prefix, mbuf, lred, hv, flag, pm, bsum, obuf, lg, total;
 };
 
 __host__ __device__ inline size_t up16(size_t x) { return (x + 15) & ~size_t(15); }
 
-__host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int cap, int n_seqs, int ns) {
+// whole: the whole-CTA plan, whose output reduction buffer reuses the ring (nothing is
+// in flight there once every consumer has finished the V pass of its one segment).
+__host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int cap, int n_seqs, int ns,
+                                             bool whole) {
   const int HQ = hkv * kG, WPK = kNCW / hkv;
   const size_t blk = (size_t)hkv * kBlock * kD * (fp8 ? 1 : 2);
   const size_t sb = kStageBytes / blk;
@@ -395,18 +462,18 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
   size_t o = 0;
   p.ring = o;   o += (size_t)ns * sb * blk;
   p.sscale = o; o += (size_t)ns * sb * kBlock * 4;
-  p.bars = o;   o += (size_t)(2 * ns + 1) * 8;                   // full, empty, append done
+  p.bars = o;   o += (size_t)(2 * ns + 2) * 8;                   // full, empty, append done, normaliser
   p.seqb = o;   o = up16(o + (size_t)n_seqs * sizeof(SeqBlocks));
-  p.blk = o;    o = up16(o + (size_t)4 * cap * 4);
+  p.blk = o;    o = up16(o + (size_t)5 * cap * 4);
   p.prefix = o; o = up16(o + (size_t)(n_seqs + 1) * 4);
   p.mbuf = o;   o += (size_t)WPK * HQ * 4;
-  p.lbuf = o;   o += (size_t)WPK * HQ * 4;
+  p.lred = o;   o += (size_t)kNCW * 32 * 4;
   p.hv = o;     o += (size_t)4 * HQ * 4;
   p.flag = o;   o += 16;
   p.pm = o;     o += (size_t)kSC * HQ * 4;
-  p.pl = o;     o += (size_t)kSC * HQ * 4;
   p.bsum = o;   o = up16(o + (size_t)cap * (HQ + 1) * 4);
-  p.obuf = o;   o += (WPK == 2 ? (size_t)hkv * 32 * 32 * 4 : 0);
+  p.obuf = whole ? p.ring : o;
+  o += (WPK == 2 && !whole ? (size_t)hkv * 32 * 32 * 4 : 0);
   p.lg = o;     o += lsmem ? (size_t)cap * (HQ * kBlock + kLgPad) * 4 : 0;
   p.total = o + 1024;                       // alignment slack
   return p;
@@ -423,7 +490,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   const int NS = P.ns;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const SmemPlan sp = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, NS);
+  const SmemPlan sp = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, NS, P.whole != 0);
   uint8_t* ring = smem + sp.ring;
   float* sscale = reinterpret_cast<float*>(smem + sp.sscale);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.bars);          // full[NS], empty[NS], app
@@ -432,16 +499,16 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   int32_t* blk_page = blk_id + P.cap;
   int32_t* blk_seq = blk_page + P.cap;
   int32_t* ticket = blk_seq + P.cap;                                   // arrival order, by segment start
+  int32_t* ppage = ticket + P.cap;                                     // whole plan: the producer's pages
   int32_t* prefix = reinterpret_cast<int32_t*>(smem + sp.prefix);       // [n_seqs + 1]
   float* mbuf = reinterpret_cast<float*>(smem + sp.mbuf);              // [WPK][HQ]
-  float* lbuf = reinterpret_cast<float*>(smem + sp.lbuf);              // [WPK][HQ]
+  float* lred = reinterpret_cast<float*>(smem + sp.lred);              // [consumer threads]
   float* mseg = reinterpret_cast<float*>(smem + sp.hv);                // [HQ]
   float* cfac = mseg + HQ;                                             // [HQ]
   float* gmax = cfac + HQ;                                             // [HQ]
   float* ginv = gmax + HQ;                                             // [HQ]
   int32_t* flag = reinterpret_cast<int32_t*>(smem + sp.flag);
   float* pm = reinterpret_cast<float*>(smem + sp.pm);                  // [kSC][HQ]
-  float* pl = reinterpret_cast<float*>(smem + sp.pl);                  // [kSC][HQ]
   float* bsum = reinterpret_cast<float*>(smem + sp.bsum);              // [cap][HQ]
   float* obuf = reinterpret_cast<float*>(smem + sp.obuf);              // WPK==2: [HKV][32][32]
   float* lg_smem = reinterpret_cast<float*>(smem + sp.lg);
@@ -449,11 +516,29 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int c = blockIdx.x, G = gridDim.x;
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + NS), app_bar = smem_u32(bars + 2 * NS);
+  const uint32_t norm_bar = smem_u32(bars + 2 * NS + 1);
+  // Whole plan with waits: the CTA holds one segment, publishes its softmax statistics
+  // (m, l) before the V pass, and the normaliser warp combines the sequence's
+  // statistics into the global normaliser while the consumers run the V pass.
+  const bool early = P.whole && d.spin_limit >= 0;
 
-  if (warp == kNCW && lane == 0) {          // fetch the two tensor maps before the first copy
+  if (warp == kProducer && lane == 0) {     // fetch the two tensor maps before the first copy
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmk)) : "memory");
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmv)) : "memory");
   }
+  // barriers touch shared memory only: set them up while the previous kernel finishes
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kNCW);      // every consumer warp releases every stage
+    }
+    mbar_init(app_bar, 1);
+    mbar_init(norm_bar, 32);                // every lane of the normaliser warp
+    flag[1] = 0;                            // normaliser valid (set by the normaliser warp)
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
 
   // everything below may read what the previous kernel of the stream wrote; let the next
   // kernel's launch begin now (it too waits for this one before reading anything)
@@ -527,7 +612,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     return;
   }
   if (cseq >= 0) {
-    for (int i = tid; i < nblk; i += kThreads) {
+    for (int i = warp < kNCW ? tid : nblk; i < nblk; i += kNCW * 32) {
       int32_t page, k;
       if (P.list_ids) {
         k = P.list_ids[(size_t)cseq * P.list_stride + x0 + i];
@@ -559,16 +644,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       blk_seq[i] = lo;
     }
   }
-  if (tid == 0) {
-    for (int s = 0; s < NS; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, kNCW);      // every consumer warp releases every stage
-    }
-    mbar_init(app_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-  }
-  __syncthreads();
+  // the split plan's lists are everybody's; the whole plan's are the consumers' (they
+  // meet at their own barrier) and the producer builds its page list itself
+  if (!P.whole) __syncthreads();
   int32_t* const ctr_base = d.counters;     // sequence s: arrivals [s * kCounterInts], departures + kDepartAt
   if (nblk == 0) {
     // A CTA of the whole plan with no block still read its sequence's next position:
@@ -578,6 +656,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       if (atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == cb - 1) {
         ctr_base[(size_t)s * kCounterInts] = 0;
         ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
+        ctr_base[(size_t)s * kCounterInts + kMlAt] = 0;
         if (P.fuse && sbw.next > 0) d.next_pos[(size_t)P.layer * d.max_seqs + s] = sbw.next;
       }
     }
@@ -589,14 +668,30 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   float* partials = d.partials;
 
   // ================================================================ producer warp
-  if (warp == kNCW) {
+  if (warp == kProducer) {
+    if (P.whole) {
+      // its own page list, so the first copies go out without waiting for the consumers
+      for (int i = lane; i < nblk; i += 32) {
+        int32_t page;
+        if (P.list_ids) {
+          int32_t k = P.list_ids[(size_t)cseq * P.list_stride + x0 + i];
+          page = list_block(d, P.seq_begin + cseq, &k);
+        } else {
+          block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+        }
+        ppage[i] = page;
+      }
+      __syncwarp();
+    }
     if (lane == 0) {
       const uint64_t pol = evict_first_policy();
+      const int32_t* pages = P.whole ? ppage : blk_page;
       uint32_t ctr = 0;
       int i0 = 0;
       while (i0 < nblk) {
         int i1 = i0 + 1;
-        while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
+        if (P.whole) i1 = nblk;                 // one segment
+        else while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
         for (int ph = 0; ph < 2; ++ph) {
           const CUtensorMap* map = ph == 0 ? &tmk : &tmv;
           const float* scales = ph == 0 ? d.k_scales : d.v_scales;
@@ -609,7 +704,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             const uint32_t fb = full0 + 8 * st;
             mbar_expect_tx(fb, nb * (C::BLK + (FP8 ? kBlock * 4 : 0)));
             for (int j = 0; j < nb; ++j) {
-              const int page = blk_page[g0 + j];
+              const int page = pages[g0 + j];
               const uint32_t dst = smem_u32(ring + (size_t)st * C::STAGE + (size_t)j * C::BLK);
               tma_load_4d(dst, map, 0, 0, 0, page, fb, pol);
               if constexpr (FP8) {
@@ -618,6 +713,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
               } else {
                 tma_load_4d(dst + C::HALF, map, 64, 0, 0, page, fb, pol);
               }
+#if KVS_VPREFETCH
+              if (ph == 0) {
+                tma_prefetch_4d(&tmv, 0, 0, 0, page);
+                if constexpr (FP8) bulk_prefetch(d.v_scales + lay_slot + (size_t)page * kBlock, kBlock * 4);
+                else tma_prefetch_4d(&tmv, 64, 0, 0, page);
+              }
+#endif
             }
           }
         }
@@ -625,10 +727,94 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       }
     }
     __syncwarp();                               // lanes 1..31 wait for the issuing lane
+    if (early) {
+      // publish the partial output rows once this CTA's consumers have written them
+      named_sync(kBarOut, kPubThreads);
+      if (lane == 0) red_release_add(ctr_base + (size_t)(P.seq_begin + cseq) * kCounterInts, 1);
+    }
+  } else if (warp == kNormWarp) {
+    // ============================================================== normaliser warp
+    if (early) {
+      // Global normaliser of the CTA's sequence, while the consumers run the V pass:
+      // wait (bounded) until every CTA of the sequence has published its statistics,
+      // then lane h merges head h's records in record order.  Record k is the
+      // sequence's k-th CTA: per head the running max m and l = sum exp2(s - m).
+      const int b = cseq, s = P.seq_begin + b;
+      const int cb = P.cst[b + 1] - P.cst[b], cf = P.cst[b];
+      const int S = sbw.n >= cb ? cb : sbw.n;
+      int ok = 1;
+      named_sync(kBarMl, kPubThreads);          // this CTA's consumers wrote its words
+      if (lane == 0) {
+        red_release_add(ctr_base + (size_t)s * kCounterInts + kMlAt, 1);
+        ok = wait_at_least(ctr_base + (size_t)s * kCounterInts + kMlAt, S, d.spin_limit) ? 1 : 0;
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (ok) {
+        const unsigned long long* rec0 = d.part_ml + (size_t)(cf + b) * HQ;   // record k, head h: [k * HQ + h]
+        const int own = c - cf;
+#pragma unroll 1
+        for (int u = 0; u < HQ / 32; ++u) {
+          const int h = lane + 32 * u;
+          if (S <= kSC) {
+            // every record in registers: one round of loads
+            unsigned long long w[kSC];
+#pragma unroll
+            for (int k = 0; k < kSC; ++k) w[k] = k < S ? __ldcg(rec0 + (size_t)k * HQ + h) : 0ull;
+            float M = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < kSC; ++k)
+              if (k < S) M = fmaxf(M, __uint_as_float((uint32_t)w[k]));
+            float Ls = 0.f;
+#pragma unroll
+            for (int k = 0; k < kSC; ++k)
+              if (k < S) Ls += __uint_as_float((uint32_t)(w[k] >> 32)) * exp2f(__uint_as_float((uint32_t)w[k]) - M);
+            const float inv = 1.0f / Ls;
+#pragma unroll
+            for (int k = 0; k < kSC; ++k) {
+              if (k < S) {
+                const float f = exp2f(__uint_as_float((uint32_t)w[k]) - M) * inv;
+                pm[k * HQ + h] = f;
+                if (k == own) cfac[h] = f;
+              }
+            }
+            gmax[h] = M;
+            ginv[h] = inv;
+          } else {
+            float M = -INFINITY, Ls = 0.f;
+            for (int k0 = 0; k0 < S; k0 += 8) {
+              unsigned long long w[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) w[j] = __ldcg(rec0 + (size_t)min(k0 + j, S - 1) * HQ + h);
+              float cm = -INFINITY;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (k0 + j < S) cm = fmaxf(cm, __uint_as_float((uint32_t)w[j]));
+              const float nm = fmaxf(M, cm);
+              float part = 0.f;
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                if (k0 + j < S) part += __uint_as_float((uint32_t)(w[j] >> 32)) * exp2f(__uint_as_float((uint32_t)w[j]) - nm);
+              Ls = Ls * exp2f(M - nm) + part;
+              M = nm;
+            }
+            const float inv = 1.0f / Ls;
+            cfac[h] = exp2f(__uint_as_float((uint32_t)__ldcg(rec0 + (size_t)own * HQ + h)) - M) * inv;
+            gmax[h] = M;
+            ginv[h] = inv;
+          }
+        }
+      } else if (lane == 0) {
+        set_error(d, kErrTimeout);
+      }
+      if (lane == 0) flag[1] = ok;
+      __syncwarp();
+      mbar_arrive(norm_bar);                    // every lane, after its own writes
+    }
   } else {
     // ============================================================== consumer warps
     const int kvh = warp % HKV, sub = warp / HKV;
     const int g = lane >> 2, t = lane & 3;
+    if (P.whole) named_sync(1, kNCW * 32);      // the block lists are written
     if (appends) {
       // fused append of position next (the state attended is next + 1): warp 0 stores K,
       // warp 1 stores V, exactly as the append kernel does; every storing lane orders its
@@ -714,10 +900,21 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       }
       named_sync(1, kNCW * 32);
 
+      // ------------------------------------------------------------ weights
+      // p = exp2(s - m) in place, block sums, and this segment's (m, l) per head as one
+      // 64-bit word in a compact array of its own, published before the V pass
+      weights_sweep<HQ>(lgbase, bsum, lred, mseg, i0, i1, tid);
+      named_sync(1, kNCW * 32);
+      if (tid < HQ) {
+        float l = 0.f;
+        for (int k = tid; k < kNCW * 32; k += HQ) l += lred[k];
+        d.part_ml[(size_t)(c + b) * HQ + tid] = ((unsigned long long)__float_as_uint(l) << 32) | __float_as_uint(mseg[tid]);
+      }
+      // whole plan: hand the words to the normaliser warp, which publishes them (no
+      // consumer waits on a fence; the producer warp does the same for the output rows)
+      if (early) named_arrive(kBarMl, kPubThreads);
+
       // ------------------------------------------------------------ pass 2: V
-      const int hg = kvh * kG + g;                 // head of this thread's P column
-      const float mh = mseg[hg];
-      float lsum = 0.f;
       float o[8][4];
 #pragma unroll
       for (int mb = 0; mb < 8; ++mb) o[mb][0] = o[mb][1] = o[mb][2] = o[mb][3] = 0.f;
@@ -729,16 +926,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const float* sst = sscale + st * C::SB * kBlock;
         int j = sub;
         for (; j + WPK < nb; j += 2 * WPK)
-          pv_blocks<HKV, FP8, 2>(stage, sst, j, g0 + j, lgbase, bsum, kvh, lane, mh, lsum, o);
+          pv_blocks<HKV, FP8, 2>(stage, sst, j, g0 + j, lgbase, kvh, lane, o);
         if (j < nb)
-          pv_blocks<HKV, FP8, 1>(stage, sst, j, g0 + j, lgbase, bsum, kvh, lane, mh, lsum, o);
+          pv_blocks<HKV, FP8, 1>(stage, sst, j, g0 + j, lgbase, kvh, lane, o);
         __syncwarp();
         if (lane == 0) mbar_arrive(empty0 + 8 * st);
       }
-      // l of head hg: sum over the four lanes sharing g
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
-      lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
-      if (t == 0) lbuf[sub * HQ + hg] = lsum;
+      if (WPK == 2 && P.whole) named_sync(1, kNCW * 32);   // the ring is free: obuf lives there
       if (WPK == 2 && sub == 1) {
 #pragma unroll
         for (int mb = 0; mb < 8; ++mb)
@@ -777,18 +971,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             rec[(size_t)(ha + 1) * kD + db] = o[mb][3];
           }
         }
-        // (m, l) of each head as one 64-bit word, in a compact array of its own
-        if (lane < kG) {
-          const int h = kvh * kG + lane;
-          float l = lbuf[h];
-          for (int w = 1; w < WPK; ++w) l += lbuf[w * HQ + h];
-          d.part_ml[(size_t)(c + b) * HQ + h] = ((unsigned long long)__float_as_uint(l) << 32) | __float_as_uint(mseg[h]);
-        }
-        // Each writer warp releases its own rows and words and arrives (HKV arrivals per
+        // Each writer warp releases its own rows and arrives (HKV arrivals per
         // CTA), without a return value: no CTA barrier on the way.  One poller per CTA
         // reads the counter (every thread polling the records themselves floods their
         // few L2 lines).
-        if (d.spin_limit >= 0) {
+        if (d.spin_limit >= 0 && !early) {
           __syncwarp();
           if (lane == 0) {
             __threadfence();
@@ -796,6 +983,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
           }
         }
       }
+      if (early) named_arrive(kBarOut, kPubThreads);   // the producer warp publishes the rows
       if (d.spin_limit < 0) {
         // nobody waits: one arrival per CTA, with its order, after a CTA barrier; only
         // the last CTA to arrive goes on
@@ -824,63 +1012,71 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         cf = cta_of(prefix[b], q, r);
         S = cta_of(prefix[b + 1] - 1, q, r) - cf + 1;
       }
-      if (tid == 0) {
-        // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
-        const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1
-                                         : wait_at_least(ctr_base + (size_t)s * kCounterInts, S * HKV, d.spin_limit);
-        flag[0] = ok ? 1 : 0;
-        if (!ok) set_error(d, kErrTimeout);
-      }
-      named_sync(1, kNCW * 32);
-      if (!flag[0]) break;
+      if (early) {
+        // the normaliser warp has combined the normaliser during the V pass: wait for it
+        // (bounded), and let every consumer thread take the same decision
+        const bool w = mbar_wait(norm_bar, 0);
+        if (!w) set_error(d, kErrTimeout);
+        if (!named_sync_and(1, kNCW * 32, w && flag[1] != 0)) break;
+      } else {
+        if (tid == 0) {
+          // spin_limit < 0: no wait at all, only the last CTA to arrive goes on
+          const bool ok = d.spin_limit < 0 ? ticket[i0] == S - 1
+                                           : wait_at_least(ctr_base + (size_t)s * kCounterInts, S * HKV, d.spin_limit);
+          flag[0] = ok ? 1 : 0;
+          if (!ok) set_error(d, kErrTimeout);
+        }
+        named_sync(1, kNCW * 32);
+        if (!flag[0]) break;
 
-      // global normaliser: warp w takes heads w, w + 8, ...; lane k reads the (m, l)
-      // word of record k (rounds of 32 records when S > 32); with S <= kSC the
-      // per-record output factors stay in pm
-      {
-        constexpr int HPW = HQ / kNCW;
-        float M[HPW], Ls[HPW], mk[HPW], mo[HPW];
-#pragma unroll
-        for (int u = 0; u < HPW; ++u) { M[u] = -INFINITY; Ls[u] = 0.f; mk[u] = -INFINITY; mo[u] = -INFINITY; }
-        for (int k0 = 0; k0 < S; k0 += 32) {
-          const int k = k0 + lane;
-          // every lane loads (lanes past S re-read record S-1 and ignore it), all loads
-          // issued before any is used
-          const unsigned long long* wp = d.part_ml + (size_t)(cf + min(k, S - 1) + b) * HQ + warp;
-          unsigned long long w[HPW];
-#pragma unroll
-          for (int u = 0; u < HPW; ++u) w[u] = __ldcg(wp + u * kNCW);
-          const int own = c - cf - k0;
-#pragma unroll
+        // global normaliser: warp w takes heads w, w + 8, ...; lane k reads the (m, l)
+        // word of record k (rounds of 32 records when S > 32); with S <= kSC the
+        // per-record output factors stay in pm
+        {
+          constexpr int HPW = HQ / kNCW;
+          float M[HPW], Ls[HPW], mk[HPW], mo[HPW];
+  #pragma unroll
+          for (int u = 0; u < HPW; ++u) { M[u] = -INFINITY; Ls[u] = 0.f; mk[u] = -INFINITY; mo[u] = -INFINITY; }
+          for (int k0 = 0; k0 < S; k0 += 32) {
+            const int k = k0 + lane;
+            // every lane loads (lanes past S re-read record S-1 and ignore it), all loads
+            // issued before any is used
+            const unsigned long long* wp = d.part_ml + (size_t)(cf + min(k, S - 1) + b) * HQ + warp;
+            unsigned long long w[HPW];
+  #pragma unroll
+            for (int u = 0; u < HPW; ++u) w[u] = __ldcg(wp + u * kNCW);
+            const int own = c - cf - k0;
+  #pragma unroll
+            for (int u = 0; u < HPW; ++u) {
+              const float m = k < S ? __uint_as_float((uint32_t)w[u]) : -INFINITY;
+              const float l = k < S ? __uint_as_float((uint32_t)(w[u] >> 32)) : 0.f;
+              float cm = m;
+  #pragma unroll
+              for (int o2 = 16; o2 > 0; o2 >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
+              const float nm = fmaxf(M[u], cm);
+              float part = l * exp2f(m - nm);              // 0 for lanes past S
+  #pragma unroll
+              for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+              Ls[u] = Ls[u] * exp2f(M[u] - nm) + part;
+              M[u] = nm;
+              mk[u] = m;
+              if (own >= 0 && own < 32) mo[u] = __shfl_sync(0xffffffffu, m, own);
+            }
+          }
+  #pragma unroll
           for (int u = 0; u < HPW; ++u) {
-            const float m = k < S ? __uint_as_float((uint32_t)w[u]) : -INFINITY;
-            const float l = k < S ? __uint_as_float((uint32_t)(w[u] >> 32)) : 0.f;
-            float cm = m;
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o2));
-            const float nm = fmaxf(M[u], cm);
-            float part = l * exp2f(m - nm);              // 0 for lanes past S
-#pragma unroll
-            for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-            Ls[u] = Ls[u] * exp2f(M[u] - nm) + part;
-            M[u] = nm;
-            mk[u] = m;
-            if (own >= 0 && own < 32) mo[u] = __shfl_sync(0xffffffffu, m, own);
+            const int h = warp + u * kNCW;
+            const float inv = 1.0f / Ls[u];
+            if (S <= kSC && lane < S) pm[lane * HQ + h] = exp2f(mk[u] - M[u]) * inv;
+            if (lane == 0) {
+              cfac[h] = exp2f(mo[u] - M[u]) * inv;
+              gmax[h] = M[u];
+              ginv[h] = inv;
+            }
           }
         }
-#pragma unroll
-        for (int u = 0; u < HPW; ++u) {
-          const int h = warp + u * kNCW;
-          const float inv = 1.0f / Ls[u];
-          if (S <= kSC && lane < S) pm[lane * HQ + h] = exp2f(mk[u] - M[u]) * inv;
-          if (lane == 0) {
-            cfac[h] = exp2f(mo[u] - M[u]) * inv;
-            gmax[h] = M[u];
-            ginv[h] = inv;
-          }
-        }
+        named_sync(1, kNCW * 32);
       }
-      named_sync(1, kNCW * 32);
       const bool fac_in_smem = S <= kSC;
 
       if (warp < kNCW / 2) {
@@ -929,12 +1125,23 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         }
         }
       } else {
+        bool out_ready = true;
+        if (early) {
+          // only the output combine needs the other CTAs' partial rows: wait for them here
+          if (warp == kNCW / 2 && lane == 0) {
+            const bool ok = wait_at_least(ctr_base + (size_t)s * kCounterInts, S, d.spin_limit);
+            flag[2] = ok ? 1 : 0;
+            if (!ok) set_error(d, kErrTimeout);
+          }
+          named_sync(kBarOutWarps, (kNCW / 2) * 32);
+          out_ready = flag[2] != 0;
+        }
         // output: this CTA combines heads h with h % S == its rank among the sequence's
         // CTAs, 4 dimensions per thread
         constexpr int D4 = kD / 4;
         constexpr size_t kRec4 = (size_t)HQ * kD / 4;      // float4 between a head's records
         const int rank = c - cf;
-        const int nh = rank < HQ ? (HQ - rank + S - 1) / S : 0;
+        const int nh = rank < HQ && out_ready ? (HQ - rank + S - 1) / S : 0;
         const int ot = tid - (kNCW / 2) * 32;
         for (int idx = ot; idx < nh * D4; idx += (kNCW / 2) * 32) {
           const int h = rank + (idx / D4) * S, d4 = idx % D4;
@@ -978,10 +1185,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       // one resets the counters.  (Issuing the departure right after the normaliser and
       // looking at its ticket only here measured 50% slower in graphs of launches.)
       named_sync(1, kNCW * 32);                    // also: the next segment reuses pm, cfac, flag
+      if (early && !flag[2]) break;                // the output wait ran out (reported)
       const int departs = P.whole ? P.cst[b + 1] - P.cst[b] : S;   // whole plan: empty CTAs depart too
       if (tid == 0 && atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == departs - 1) {
         ctr_base[(size_t)s * kCounterInts] = 0;    // last CTA of the sequence to leave
         ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
+        ctr_base[(size_t)s * kCounterInts + kMlAt] = 0;
         if (P.fuse) d.next_pos[(size_t)P.layer * d.max_seqs + s] = sb.next;   // every reader is done
       }
       i0 = i1;
@@ -993,11 +1202,11 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
 size_t tc_smem_limit() { return 227 * 1024; }
 
 // Ring stages that fit next to the rest of the carve-up (0 if fewer than kMinStages).
-int ring_stages(int hkv, bool fp8, bool lsmem, int cap, int n_seqs) {
+int ring_stages(int hkv, bool fp8, bool lsmem, int cap, int n_seqs, bool whole) {
   const size_t blk = (size_t)hkv * kBlock * kD * (fp8 ? 1 : 2);
   const size_t sb = kStageBytes / blk;
   const size_t stage = sb * blk;
-  const size_t rest = plan_smem(hkv, fp8, lsmem, cap, n_seqs, 0).total;
+  const size_t rest = plan_smem(hkv, fp8, lsmem, cap, n_seqs, 0, whole).total;
   if (rest >= tc_smem_limit()) return 0;
   size_t ns = (tc_smem_limit() - rest) / (stage + sb * kBlock * 4 + 16);
   ns = ns < (size_t)(kRingBytes / stage) ? ns : (size_t)(kRingBytes / stage);
@@ -1008,7 +1217,7 @@ template <int HKV, bool FP8, bool LSMEM>
 cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, const Params& P, int grid,
                        cudaStream_t st) {
   auto fn = attend_tc_kernel<HKV, FP8, LSMEM>;
-  const size_t smem = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, P.ns).total;
+  const size_t smem = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, P.ns, P.whole != 0).total;
   static bool attr_set = false;      // one opt-in per instantiation, to the full limit
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_limit());
@@ -1073,9 +1282,9 @@ bool plan_whole(Params& P, const int32_t* bounds, int grid, int cap_limit) {
 template <int HKV, bool FP8>
 cudaError_t launch_pick(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, Params P, int grid,
                         cudaStream_t st) {
-  P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs);
+  P.ns = ring_stages(HKV, FP8, true, P.cap, P.n_seqs, P.whole != 0);
   if (P.ns > 0) return launch_one<HKV, FP8, true>(tk, tv, d, P, grid, st);
-  P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs);
+  P.ns = ring_stages(HKV, FP8, false, P.cap, P.n_seqs, P.whole != 0);
   if (P.ns == 0) return cudaErrorInvalidConfiguration;
   if ((size_t)grid * P.cap * lg_block<Cfg<HKV, FP8>::HQ>() > d.logit_scratch_elems) return cudaErrorInvalidConfiguration;
   return launch_one<HKV, FP8, false>(tk, tv, d, P, grid, st);
@@ -1260,13 +1469,13 @@ cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv
   const bool fp8 = d.kv_dtype == KVS_E4M3;
   P.ns = 0;
   if (plan_whole(P, bounds, grid, wide_cap(cap0))) {
-    P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+    P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs, true);
     if (P.ns == 0) {
       P.whole = 0;
       P.cap = cap0;
     }
   }
-  if (P.ns == 0) P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs);
+  if (P.ns == 0) P.ns = ring_stages(d.Hkv, fp8, true, P.cap, n_seqs, P.whole != 0);
   if (P.ns == 0) return cudaErrorNotSupported;
   void* base = nullptr;
   cudaError_t e = static_scratch_address(&base);

@@ -41,11 +41,13 @@ enum : int32_t {
   kErrState = 4,         // missing page / inconsistent state seen on device
 };
 
-// The attend's per-sequence arrival and departure counters each sit on a 128-byte line
-// of their own: every CTA of a sequence polls the arrival count, and counters of
-// several sequences on one line made all pollers and all atomics contend for it.
-constexpr int kCounterInts = 64;
+// The attend's per-sequence counters each sit on a 128-byte line of their own: every
+// CTA of a sequence polls them, and counters of several sequences on one line made all
+// pollers and all atomics contend for it.  Output arrivals at 0, departures at
+// kDepartAt, softmax-statistics arrivals at kMlAt.
+constexpr int kCounterInts = 96;
 constexpr int kDepartAt = 32;
+constexpr int kMlAt = 64;
 
 // Options of a tensor-core attend launch (all off by default).
 struct AttendOpts {
@@ -96,7 +98,8 @@ struct Dev {
   int32_t* acc_tickets;                              // [max_seqs]
   float* partials;        // [records][Hq][D] partial output rows, records = kGridMax + max_seqs
   unsigned long long* part_ml;   // [records][Hq] softmax partials (l bits << 32 | m bits)
-  int32_t* counters;      // [max_seqs][kCounterInts]: arrivals at 0, departures at kDepartAt
+  int32_t* counters;      // [max_seqs][kCounterInts]: arrivals at 0, departures at kDepartAt,
+                          // statistics arrivals at kMlAt
   float* logit_scratch;   size_t logit_scratch_elems;
   int32_t* err;           // [1]
 };
