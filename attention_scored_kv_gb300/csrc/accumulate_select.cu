@@ -109,11 +109,12 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
   const bool keep_all = kk >= n;
   int rank = 0;
   if (tid < n && !keep_all) {
+    // keys above ki, and equal keys of lower ids: split at tid, one compare per key
     const uint64_t ki = skey[tid];
-    for (int c = 0; c < n; ++c) {
-      const uint64_t kc = skey[c];
-      rank += (kc > ki || (kc == ki && c < tid)) ? 1 : 0;
-    }
+#pragma unroll 4
+    for (int c = 0; c < tid; ++c) rank += skey[c] >= ki ? 1 : 0;
+#pragma unroll 4
+    for (int c = tid + 1; c < n; ++c) rank += skey[c] > ki ? 1 : 0;
   }
   const int keep = (tid < n && (keep_all || rank < kk)) ? 1 : 0;
   int kept = 0;

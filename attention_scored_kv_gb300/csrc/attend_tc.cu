@@ -415,6 +415,7 @@ struct Params {
   // the plan stays valid; whole == 0 leaves the split to the device.
   int whole;
   int cst[kGridMax + 1];
+  uint8_t cta_seq[kGridMax];           // whole plan: the b with cst[b] <= c < cst[b + 1]
   // Fused append (whole plan only): before attending, store one new token per sequence,
   // K and V rows [n_seqs][Hkv][D] in the input dtype, at position next_position.
   int fuse;
@@ -554,11 +555,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   bool appends = false;                     // fused append: this CTA stores the new token
   if (P.whole) {
     if (c < P.cst[P.n_seqs]) {
-      int lo = 0, hi = P.n_seqs - 1;        // last b with cst[b] <= c
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (P.cst[mid] <= c) lo = mid; else hi = mid - 1;
-      }
+      const int lo = P.cta_seq[c];          // one lookup (a search costs a chain of loads)
       wseq = lo;
       int64_t nxt = d.next_pos[(size_t)P.layer * d.max_seqs + P.seq_begin + lo];
       // fused append: attend over the state after the new position (the host checked the
@@ -734,6 +731,31 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     }
   } else if (warp == kNormWarp) {
     // ============================================================== normaliser warp
+    if (appends) {
+      // fused append of position next (the state attended is next + 1), stored exactly
+      // as the append kernel does while the consumers already run the K pass; the
+      // producer copies the newest block only after app_bar.  Every storing lane orders
+      // its generic-proxy stores before those copies.
+      const int s = P.seq_begin + cseq;
+      const int64_t pnew = sbw.next - 1;
+      int32_t slot;
+      const int32_t page = page_of(d, s, pnew, &slot);
+      const size_t src_elem = (size_t)cseq * d.Hkv * d.D;
+      const size_t lay_slot0 = (size_t)P.layer * d.slot_layer_elems + (size_t)page * kBlock;
+      for (int kv = 0; kv < 2; ++kv) {
+        uint8_t* base = (kv == 0 ? d.k_pages : d.v_pages) + P.layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
+        float* scales = kv == 0 ? d.k_scales : d.v_scales;
+        store_position<FP8 ? KVS_E4M3 : KVS_BF16, KVS_BF16>(d, kv == 0 ? P.k_new : P.v_new, src_elem, base,
+                                                          scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
+      }
+      if (lane == 0) d.pos[lay_slot0 + slot] = pnew;
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        mbar_arrive(app_bar);
+      }
+    }
     if (early) {
       // Global normaliser of the CTA's sequence, while the consumers run the V pass:
       // wait (bounded) until every CTA of the sequence has published its statistics,
@@ -815,30 +837,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     const int kvh = warp % HKV, sub = warp / HKV;
     const int g = lane >> 2, t = lane & 3;
     if (P.whole) named_sync(1, kNCW * 32);      // the block lists are written
-    if (appends) {
-      // fused append of position next (the state attended is next + 1): warp 0 stores K,
-      // warp 1 stores V, exactly as the append kernel does; every storing lane orders its
-      // generic-proxy stores before the copies the producer issues after app_bar
-      const int s = P.seq_begin + cseq;
-      const int64_t pnew = sbw.next - 1;
-      if (warp < 2) {
-        int32_t slot;
-        const int32_t page = page_of(d, s, pnew, &slot);
-        const size_t src_elem = (size_t)cseq * d.Hkv * d.D;
-        const size_t lay_slot0 = (size_t)P.layer * d.slot_layer_elems + (size_t)page * kBlock;
-        uint8_t* base = (warp == 0 ? d.k_pages : d.v_pages) + P.layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
-        float* scales = warp == 0 ? d.k_scales : d.v_scales;
-        store_position<FP8 ? KVS_E4M3 : KVS_BF16, KVS_BF16>(d, warp == 0 ? P.k_new : P.v_new, src_elem, base,
-                                                          scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
-        if (warp == 0 && lane == 0) d.pos[lay_slot0 + slot] = pnew;
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
-      named_sync(1, kNCW * 32);
-      if (tid == 0) {
-        __threadfence();
-        mbar_arrive(app_bar);
-      }
-    }
     uint32_t ctr = 0;
     int i0 = 0;
     while (i0 < nblk) {
@@ -1271,6 +1269,7 @@ bool plan_whole(Params& P, const int32_t* bounds, int grid, int cap_limit) {
   int run = 0;
   for (int b = 0; b < P.n_seqs; ++b) {
     P.cst[b] = run;
+    for (int x = run; x < run + (bounds[b] + lo - 1) / lo && x < kGridMax; ++x) P.cta_seq[x] = (uint8_t)b;
     run += (bounds[b] + lo - 1) / lo;
   }
   P.cst[P.n_seqs] = run;

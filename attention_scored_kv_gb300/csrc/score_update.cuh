@@ -27,11 +27,22 @@ __device__ __forceinline__ double decayed(double e, int32_t last, int32_t step, 
 }
 
 // Entry p of sequence s, stored in (page, slot), at step `step`; returns its score x.
+// The layer sum runs in float32 as an unevaluated pair hi + lo kept exact by the
+// two-sum rule (Knuth: s = a + b, bb = s - a, err = (a - (s - bb)) + (b - bb), so that
+// s + err == a + b exactly), and becomes one float64 at the end: this part's float64
+// rate is low, and ten float64 conversions and adds per entry dominated the update.
+// The pair carries about 48 bits, beyond the float64 tables' 1e-4 absolute bar.
 __device__ __forceinline__ double update_entry(const Dev& d, int s, int64_t p, int32_t page, int32_t slot,
                                                int32_t step) {
-  double x = 0.0;
-  for (int l = 0; l < d.L; ++l)
-    x += (double)d.tok_mass[(size_t)l * d.slot_layer_elems + (size_t)page * kBlock + slot];
+  float hi = 0.f, lo = 0.f;
+  for (int l = 0; l < d.L; ++l) {
+    const float v = d.tok_mass[(size_t)l * d.slot_layer_elems + (size_t)page * kBlock + slot];
+    const float t = __fadd_rn(hi, v);
+    const float bb = __fsub_rn(t, hi);
+    lo = __fadd_rn(lo, __fadd_rn(__fsub_rn(hi, __fsub_rn(t, bb)), __fsub_rn(v, bb)));
+    hi = t;
+  }
+  const double x = (double)hi + (double)lo;
   const size_t t = (size_t)s * d.max_positions + p;
   const int32_t last = d.last_tok[t];
   const double e_prev = decayed(d.e_tok[t], last, step, d.ema_decay);
