@@ -6,12 +6,11 @@
 // SMs matters here, because this part's FP64 rate is low. Each CTA takes a ticket.
 // The last CTA of a sequence to finish then selects for it, with the select kernel's
 // keys (select_key.cuh), read through L2 because other CTAs have just written them.
-// The k-th best is found by ranking. Candidate i's rank is the number of keys above
-// it plus the number of equal keys with a lower id; candidates are enumerated in
-// ascending block id. The candidates with rank < k are the set the select kernel's
-// radix select keeps: every key above the k-th best, then the first ties by id. A
-// stable compaction writes them in id order, and H2O eviction rewrites the resident
-// list as the select kernel does.
+// Candidates are enumerated in ascending block id, one per thread. The kept set is the
+// candidates whose rank (keys above plus equal keys of lower id) is below k, found as
+// the select kernel finds it: a radix select gives the k-th best key T, and the set is
+// every key above T, then the first ties with T by id. A stable compaction writes them
+// in id order, and H2O eviction rewrites the resident list as the select kernel does.
 #include "score_update.cuh"
 #include "select_key.cuh"
 
@@ -48,6 +47,10 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
   __shared__ int32_t sid[kRankMax], spage[kRankMax];
   __shared__ int32_t warp_sums[kThreads / 32];
   __shared__ int32_t is_last;
+  __shared__ uint32_t hist[256];
+  __shared__ uint64_t s_prefix;
+  __shared__ int32_t s_take;
+  const int lane_id = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
   const int sl = blockIdx.y, s = seq_begin + sl, tid = threadIdx.x;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
@@ -107,16 +110,60 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
   if (kk < 0) kk = 0;
   if (kk < n_prot) kk = n_prot;
   const bool keep_all = kk >= n;
-  int rank = 0;
-  if (tid < n && !keep_all) {
-    // keys above ki, and equal keys of lower ids: split at tid, one compare per key
-    const uint64_t ki = skey[tid];
-#pragma unroll 4
-    for (int c = 0; c < tid; ++c) rank += skey[c] >= ki ? 1 : 0;
-#pragma unroll 4
-    for (int c = tid + 1; c < n; ++c) rank += skey[c] > ki ? 1 : 0;
+  // Radix select, most significant byte first: T = the kk-th best key and take = how
+  // many keys equal to T are kept.  Kept: every key above T, then the first take keys
+  // equal to T in id order (thread order).  That is the set whose rank (keys above plus
+  // equal keys of lower id) is below kk.
+  if (tid == 0) {
+    s_prefix = 0;
+    s_take = kk;
   }
-  const int keep = (tid < n && (keep_all || rank < kk)) ? 1 : 0;
+  uint64_t mask = 0;
+  if (!keep_all && kk > 0) {
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      const uint64_t prefix = s_prefix;
+      if (tid < n && (skey[tid] & mask) == prefix) atomicAdd(&hist[(skey[tid] >> shift) & 255u], 1u);
+      __syncthreads();
+      if (warp_id == 0) {
+        // lane l holds buckets 255-8l .. 248-8l (descending); the lane whose range holds
+        // the take-th largest key finds its bucket
+        const int rem = s_take;
+        int c8[8], local = 0;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          c8[u] = (int)hist[255 - 8 * lane_id - u];
+          local += c8[u];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int v = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane_id >= o) incl += v;
+        }
+        const int excl = incl - local;
+        if (excl < rem && rem <= incl) {
+          int acc = excl;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (acc < rem && acc + c8[u] >= rem) {
+              s_prefix = prefix | ((uint64_t)(255 - 8 * lane_id - u) << shift);
+              s_take = rem - acc;
+            }
+            acc += c8[u];
+          }
+        }
+      }
+      __syncthreads();
+      mask |= 0xFFull << shift;
+    }
+  }
+  const uint64_t T = s_prefix;
+  const bool is_t = !keep_all && kk > 0 && tid < n && skey[tid] == T;
+  int n_eq = 0;
+  const int eq_before = scan_flags(is_t ? 1 : 0, warp_sums, &n_eq);
+  const int keep = (tid < n && (keep_all || (kk > 0 && (skey[tid] > T || (is_t && eq_before < s_take))))) ? 1 : 0;
   int kept = 0;
   const int out = scan_flags(keep, warp_sums, &kept);   // candidates in id order = thread order
   if (tid < n) {
