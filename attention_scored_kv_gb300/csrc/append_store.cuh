@@ -85,4 +85,66 @@ __device__ void store_position(const Dev& d, const void* src, size_t src_elem, u
   }
 }
 
+// The same store for bf16 input already in registers: lane l holds chunks l, l + 32,
+// ... (NCH of them, 8 values each) of the position's Hkv*D values, loaded by
+// load_position_bf16.  Same arithmetic as store_position<KV, KVS_BF16>, so the bytes
+// are the same.  Used by the fused append, which loads the rows before its own copies
+// fill the memory queue.
+template <int NCH>
+__device__ __forceinline__ void load_position_bf16(const void* src, size_t src_elem, int lane, uint4 (&raw)[NCH]) {
+#pragma unroll
+  for (int j = 0; j < NCH; ++j)
+    raw[j] = *reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + src_elem + (size_t)(lane + 32 * j) * 8);
+}
+
+template <int KV, int NCH>
+__device__ void store_position_regs(const Dev& d, const uint4 (&raw)[NCH], uint8_t* page_base, float* scale_slot,
+                                    int slot, int lane) {
+  if constexpr (KV == KVS_E4M3) {
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        amax = fmaxf(amax, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float scale = (amax > 0.f) ? __fdiv_rn(amax, 240.0f) : 0.f;
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        v[2 * i] = f.x;
+        v[2 * i + 1] = f.y;
+      }
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        uint32_t code = 0;
+        if (scale > 0.f)
+          code = (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(v[i], scale), __NV_SATFINITE, __NV_E4M3);
+        if (i < 4) lo |= code << (8 * i); else hi |= code << (8 * (i - 4));
+      }
+      const int e = (lane + 32 * j) * 8, kvh = e / d.D, dd = e % d.D;
+      uint8_t* dst = page_base + ((size_t)(kvh * kBlock + slot) * d.D + dd);
+      *reinterpret_cast<uint2*>(dst) = make_uint2(lo, hi);
+    }
+    if (lane == 0) *scale_slot = scale;
+  } else {
+    static_assert(KV == KVS_BF16, "bf16 or E4M3 storage");
+#pragma unroll
+    for (int j = 0; j < NCH; ++j) {
+      const int e = (lane + 32 * j) * 8, kvh = e / d.D, dd = e % d.D;
+      *reinterpret_cast<uint4*>(page_base + ((size_t)(kvh * kBlock + slot) * d.D + dd) * 2) = raw[j];
+    }
+  }
+}
+
 }  // namespace kvs

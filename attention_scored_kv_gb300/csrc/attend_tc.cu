@@ -546,6 +546,22 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+  // Fused append: the normaliser warp of the CTA that will hold the newest block (the
+  // sequence's last CTA when every CTA has blocks) reads the new K and V rows now,
+  // before this SM's copies queue up ahead of any load.
+  constexpr int kNch = HKV * kD / 8 / 32;   // 8-value chunks per lane of one position
+  uint4 knew[kNch], vnew[kNch];
+  bool preloaded = false;
+  if (P.fuse && warp == kNormWarp && c < P.cst[P.n_seqs]) {
+    const int b = P.cta_seq[c];
+    if (c == P.cst[b + 1] - 1) {
+      const size_t src_elem = (size_t)b * HKV * kD;
+      load_position_bf16(P.k_new, src_elem, lane, knew);
+      load_position_bf16(P.v_new, src_elem, lane, vnew);
+      preloaded = true;
+    }
+  }
+
   // ---------------------------------------------------------------- partition
   int x0 = 0;                               // whole plan: block index within the sequence
   int nblk = 0, cseq = -1;                  // cseq: the CTA's one sequence (whole plan)
@@ -740,13 +756,17 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const int64_t pnew = sbw.next - 1;
       int32_t slot;
       const int32_t page = page_of(d, s, pnew, &slot);
-      const size_t src_elem = (size_t)cseq * d.Hkv * d.D;
+      const size_t src_elem = (size_t)cseq * HKV * kD;
       const size_t lay_slot0 = (size_t)P.layer * d.slot_layer_elems + (size_t)page * kBlock;
+      if (!preloaded) {                         // (a sequence with fewer blocks than CTAs)
+        load_position_bf16(P.k_new, src_elem, lane, knew);
+        load_position_bf16(P.v_new, src_elem, lane, vnew);
+      }
       for (int kv = 0; kv < 2; ++kv) {
         uint8_t* base = (kv == 0 ? d.k_pages : d.v_pages) + P.layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
         float* scales = kv == 0 ? d.k_scales : d.v_scales;
-        store_position<FP8 ? KVS_E4M3 : KVS_BF16, KVS_BF16>(d, kv == 0 ? P.k_new : P.v_new, src_elem, base,
-                                                          scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
+        store_position_regs<FP8 ? KVS_E4M3 : KVS_BF16>(d, kv == 0 ? knew : vnew, base,
+                                                        scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
       }
       if (lane == 0) d.pos[lay_slot0 + slot] = pnew;
       asm volatile("fence.proxy.async.global;" ::: "memory");
