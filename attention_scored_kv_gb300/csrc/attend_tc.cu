@@ -10,28 +10,36 @@
 // sum_h a_hj and the block mass max_h sum_{j in block} a_hj.
 //
 // How (GB300):
-//   * Persistent, cooperative grid of one CTA per SM.  The resident 16-token blocks of
-//     all sequences of the launch are laid end to end and split evenly over the CTAs,
-//     so a ragged batch balances by construction; a CTA's share is cut into segments
-//     (runs of blocks of one sequence).
-//   * One producer warp streams each block's K (then V) for all KV heads into a ring
-//     of shared-memory stages (up to 128 KB, as deep as the free shared memory allows)
-//     with TMA tensor copies (128-byte swizzle, L2 evict-first) completed on mbarriers;
-//     E4M3 scales arrive by bulk copy on the same barrier.
-//   * Eight consumer warps, each bound to one KV head, run QK^T and PV on the tensor
-//     cores with mma.sync m16n8k16 (positions on M, the 8 heads of the group on N for
-//     QK^T; dimensions on M for PV).  E4M3 codes are decoded to f16 in registers
-//     (exact) and fed straight into the MMA fragments; the K scale is applied to the
-//     fp32 logits, the V scale is folded into P.  bf16 P is split in two bf16 terms
-//     (hi + lo) so the PV product keeps ~16 bits.
+//   * Persistent, cooperative grid of one CTA per SM.  When every sequence can have CTAs
+//     of its own, the host plans whole CTAs per sequence (sequence b owns CTAs
+//     [cst[b], cst[b+1]) and splits its blocks evenly over them, one segment per CTA);
+//     otherwise the resident 16-token blocks of all sequences are laid end to end and
+//     split evenly over the CTAs on the device, a CTA's share cut into segments (runs
+//     of blocks of one sequence).
+//   * Ten warps.  One producer warp streams each block's K (then V) for all KV heads
+//     into a ring of 48 KB shared-memory stages (three in the whole-CTA plan) with TMA
+//     tensor copies (128-byte swizzle, L2 evict-first) completed on mbarriers; E4M3
+//     scales arrive by bulk copy on the same barrier.  In the whole-CTA plan it builds
+//     its own page list and issues the first copies without waiting for the consumers.
+//   * Eight consumer warps, one or two per KV head, run QK^T and PV on the tensor cores
+//     with mma.sync m16n8k16 (positions on M, the 8 heads of the group on N for QK^T;
+//     dimensions on M for PV).  E4M3 codes are decoded to f16 in registers (exact) and
+//     fed straight into the MMA fragments; the K scale is applied to the fp32 logits,
+//     the V scale is folded into P.  bf16 P is split in two bf16 terms (hi + lo) so the
+//     PV product keeps ~16 bits.
 //   * Two passes per segment: all K blocks first (logits to shared memory, exact local
-//     max), then all V blocks (p = exp2(s - m), written back in place, and PV) - no
-//     rescaling of accumulators.
-//   * Each CTA publishes its partial output rows and (m, l) words per head and segment,
-//     arrives on a per-sequence counter, waits (bounded) until every CTA of the sequence
-//     has arrived, combines the global normaliser, converts its own on-chip p into the
-//     final weights and reduces them to the entry and block masses; the CTAs of a
-//     sequence share the output combine.  The last CTA to leave resets the counters.
+//     max), then the weights p = exp2(s - m) in place with the block sums and l, and
+//     the CTA's (m, l) words are published; then all V blocks (PV) - no rescaling of
+//     accumulators.
+//   * The tenth warp (whole-CTA plan) stores the fused append's decode token while the
+//     consumers run the K pass, then combines the sequence's normaliser from every
+//     CTA's (m, l) words while they run the V pass.  Consumers hand their words and
+//     partial output rows over with non-blocking named-barrier arrivals; this warp and
+//     the producer publish them with one release-add per CTA on the sequence's counters.
+//   * Epilogue: four consumer warps turn the CTA's own on-chip p into the final weights
+//     and reduce them to the entry and block masses; the other four wait (bounded) for
+//     every CTA's partial rows and share the output combine.  The last CTA to leave
+//     resets the counters (and, for the fused append, advances the next position).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
