@@ -220,7 +220,8 @@ KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  * this is a deployment variant, not a step of the method.
  *
  * The tensor-core attend needs a per-launch exchange area (one softmax partial per
- * CTA and sequence, two arrival counters per sequence).  kvs_decode_attend keeps it in
+ * CTA and sequence, three counters per sequence: output arrivals, statistics arrivals
+ * and departures).  kvs_decode_attend keeps it in
  * the context's workspace.  This entry point instead uses one fixed array of 8 MiB
  * compiled into the library (a __device__ array each GPU that loads the library holds
  * until the process exits), so the call itself needs no device memory beyond the
@@ -236,7 +237,7 @@ KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  *   KVS_ERR_CAPACITY     the launch needs more than the array holds:
  *                        (grid + n_seqs) * num_q_heads * head_dim * 4 bytes,
  *                        rounded up to 256, plus (grid + n_seqs) * num_q_heads * 8
- *                        rounded up to 256, plus 256 * max_seqs bytes must be
+ *                        rounded up to 256, plus 384 * max_seqs bytes must be
  *                        <= 8 MiB.
  * The array is shared by every call of every context on the device and keeps the last
  * call's contents; the counters are cleared on `stream` before each launch.  Two such
