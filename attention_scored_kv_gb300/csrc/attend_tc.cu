@@ -489,8 +489,8 @@ __host__ __device__ inline SmemPlan plan_smem(int hkv, bool fp8, bool lsmem, int
 }
 
 template <int HKV, bool FP8, bool LSMEM>
-// 9 warps: one of the 4 schedulers holds 3 of them, and each scheduler has 16K registers,
-// so 168 per thread is the most one CTA per SM can have
+// 10 warps: two of the 4 schedulers hold 3 of them, and each scheduler has 16K
+// registers, so 168 per thread is the most one CTA per SM can have
 __global__ void __maxnreg__(168)
 attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                  const Dev d, const Params P) {
@@ -1423,7 +1423,7 @@ int tc_grid(int kv_dtype, int Hkv, int sm_count) {
 // Tensor-core attend with its exchange area in a library-owned array.
 //
 // The attend launch needs an exchange area: one (m, l, o) record per CTA and sequence
-// and two arrival counters per sequence.  kvs_decode_attend takes it from the caller's
+// and three counters per sequence (output arrivals, statistics arrivals, departures).  kvs_decode_attend takes it from the caller's
 // workspace; this variant takes it from the array below, compiled into the library, so
 // a call asks the caller for nothing but its inputs and outputs.  The array holds
 // kStaticScratchBytes; a launch that needs more is refused.  Every call (every context,
