@@ -45,6 +45,9 @@
 #include <cuda_fp16.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "append_store.cuh"
 #include "kvs_internal.cuh"
 
@@ -114,18 +117,6 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;"
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(bar), "l"(policy)
       : "memory");
-}
-#ifndef KVS_VPREFETCH
-#define KVS_VPREFETCH 0
-#endif
-// L2 prefetches: hints only, nothing lands in shared memory and nothing completes on a
-// barrier.  The tensor form is bounds-checked against the map like a load.
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];"
-               :: "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
-}
-__device__ __forceinline__ void bulk_prefetch(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
@@ -734,13 +725,6 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
               } else {
                 tma_load_4d(dst + C::HALF, map, 64, 0, 0, page, fb, pol);
               }
-#if KVS_VPREFETCH
-              if (ph == 0) {
-                tma_prefetch_4d(&tmv, 0, 0, 0, page);
-                if constexpr (FP8) bulk_prefetch(d.v_scales + lay_slot + (size_t)page * kBlock, kBlock * 4);
-                else tma_prefetch_4d(&tmv, 64, 0, 0, page);
-              }
-#endif
             }
           }
         }
@@ -1244,12 +1228,9 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
                        cudaStream_t st) {
   auto fn = attend_tc_kernel<HKV, FP8, LSMEM>;
   const size_t smem = plan_smem(HKV, FP8, LSMEM, P.cap, P.n_seqs, P.ns, P.whole != 0).total;
-  static bool attr_set = false;      // one opt-in per instantiation, to the full limit
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc_smem_limit());
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> optin{0};   // per device: opt-in to the full limit
+  const cudaError_t oe = smem_optin_once(optin, fn, (int)tc_smem_limit());
+  if (oe != cudaSuccess) return oe;
   if (smem > tc_smem_limit()) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -1328,13 +1309,17 @@ bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window
 
 // Tensor map over one layer's pages viewed as [num_pages][Hkv][16][D] elements.
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype) {
-  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  // the driver entry point is looked up once; threads racing on the first lookup store
+  // the same pointer
+  static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> encode_fn{nullptr};
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn.load(std::memory_order_acquire);
   if (!encode) {
     cudaDriverEntryPointQueryResult qr;
     void* fn = nullptr;
     cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
     if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    encode_fn.store(encode, std::memory_order_release);
   }
   const bool fp8 = kv_dtype == KVS_E4M3;
   const int esz = fp8 ? 1 : 2;
@@ -1435,7 +1420,10 @@ static __device__ __align__(256) unsigned char g_attend_scratch[kStaticScratchBy
 
 namespace {
 constexpr int kMaxDevices = 64;
-void* g_scratch_addr[kMaxDevices] = {};
+// Device address of the array per device: filled under the mutex on a device's first
+// call, read without it afterwards.
+std::atomic<void*> g_scratch_addr[kMaxDevices];
+std::mutex g_scratch_mu;
 }  // namespace
 
 size_t static_scratch_limit() { return kStaticScratchBytes; }
@@ -1458,13 +1446,19 @@ cudaError_t static_scratch_address(void** out) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_attend_scratch);
-    if (e != cudaSuccess) return e;
-    g_scratch_addr[dev] = p;
+  void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    // one lookup per device even when several host threads make their first call at
+    // once; a failed lookup is not kept, so a later call tries again
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    p = g_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      e = cudaGetSymbolAddress(&p, g_attend_scratch);
+      if (e != cudaSuccess) return e;
+      g_scratch_addr[dev].store(p, std::memory_order_release);
+    }
   }
-  *out = g_scratch_addr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

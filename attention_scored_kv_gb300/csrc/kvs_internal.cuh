@@ -182,7 +182,24 @@ __device__ __forceinline__ bool wait_at_least(const int32_t* p, int32_t target, 
 }  // namespace kvs
 
 // Host-side entry points of each translation unit (launchers).
+#include <atomic>
 namespace kvs {
+// Dynamic shared-memory opt-in of kernel `fn` to `bytes` on the current device, made
+// once per device: the attribute is per device, so `done` keeps one bit per device
+// (devices 0..63; others set it on every call).  Two host threads that race on a
+// device's first call may both make the call, which sets the same value.
+template <typename Kernel>
+inline cudaError_t smem_optin_once(std::atomic<unsigned long long>& done, Kernel fn, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
+
 struct Ctx;
 cudaError_t launch_init(const Dev& d, cudaStream_t st);
 cudaError_t launch_reset(const Dev& d, int seq_begin, int n_seqs, cudaStream_t st);

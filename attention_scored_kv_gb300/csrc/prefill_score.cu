@@ -21,7 +21,8 @@
 //     one thread.  The 128 x 64 fp32 logits of each half land in TMEM, which holds two
 //     stages so the MMA of stage s + 1 overlaps the epilogue of stage s.  Four epilogue
 //     warps, one TMEM lane each per row, also stage the keys: bf16 as is, E4M3 decoded
-//     to f16 (exact), with the queries rounded to f16 as the decode attend does.  Each
+//     to f16 (exact), with the bf16 queries converted to f16 as the decode attend does
+//     (exact in f16's normal range).  Each
 //     stage's global loads are issued one stage ahead, into registers.
 //   * pass 1 (stats): each row keeps its running max and sum of exp2 over the chunk.
 //   * combine: one thread per (sequence, head, row) merges the chunks into max, 1/sum.
@@ -575,16 +576,10 @@ size_t tc_smem(int pass, int chunk_blocks) {
 
 template <bool FP8>
 cudaError_t launch_ps(const PSArgs& A, int n_seqs, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(ps_tc_kernel<FP8, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)tc_smem(1, kPrefillChunkMax));
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(ps_tc_kernel<FP8, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)tc_smem(2, kPrefillChunkMax));
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> optin1{0}, optin2{0};   // per device
+  cudaError_t e = smem_optin_once(optin1, ps_tc_kernel<FP8, 1>, (int)tc_smem(1, kPrefillChunkMax));
+  if (e == cudaSuccess) e = smem_optin_once(optin2, ps_tc_kernel<FP8, 2>, (int)tc_smem(2, kPrefillChunkMax));
+  if (e != cudaSuccess) return e;
   const dim3 grid(A.n_chunks, A.d.Hkv, n_seqs);
   ps_tc_kernel<FP8, 1><<<grid, PT<1>::THREADS, tc_smem(1, A.chunk_blocks), st>>>(A);
   const int rows = n_seqs * A.d.Hq * kObs;

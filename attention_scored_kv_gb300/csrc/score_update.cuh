@@ -6,8 +6,9 @@
 // step.  Flash-MoE "Context Optimization", H2O > How It Works, step 1: the token score
 // sums the post-softmax weights over all heads (and, here, all layers) and all steps.
 // "Per-Head Attention as a Scoring Signal": the block score is the maximum over heads
-// (and layers).  Token score x_p = sum_l tau_l[p] (float64 sum of the float32 layer
-// masses, layers in order); block score y_k = max_l beta_l[k]; C += x;
+// (and layers).  Token score x_p = sum_l tau_l[p] (the float32 layer masses added in
+// layer order as an exact float32 two-sum pair hi + lo, converted to float64 once at
+// the end); block score y_k = max_l beta_l[k]; C += x;
 // E <- d*E + (1-d)*x.  The decay of entries not updated for a while is applied lazily:
 // each entry keeps the step at which E was last written and a reader multiplies by
 // d^(steps elapsed).

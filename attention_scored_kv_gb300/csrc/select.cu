@@ -218,12 +218,9 @@ cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
                           int32_t* keep_count, cudaStream_t st) {
   const size_t smem = (size_t)kSmemCap * (8 + 4 + 4);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> optin{0};   // per device
+  const cudaError_t e = smem_optin_once(optin, select_kernel, (int)smem);
+  if (e != cudaSuccess) return e;
   select_kernel<<<n_seqs, kThreads, smem, st>>>(d, seq_begin, k_per_seq, k_uniform, score_kind, flags, keep_ids,
                                                 keep_capacity, keep_count);
   return cudaGetLastError();

@@ -599,14 +599,19 @@ def run_reference(args, world, rank):
         if i >= args.warmup:
             times.append(dt)
     per_layer_seq = sum(times) / len(times)
-    step_s = per_layer_seq * wl.num_layers * wl.batch
+    factor = wl.num_layers * wl.batch                # samples in one decode step of the workload
+    step_s = per_layer_seq * factor
     value = 1.0 / step_s
-    sample = ("each step: one layer of one sequence (append + attend over %d entries; the sequence's "
-              "accumulate + select on every %d-th), extrapolated x%d layers x%d sequences" % (
+    sample = ("each timed step: one layer of one sequence (append + attend over %d entries; the sequence's "
+              "accumulate + select on every %d-th); value = 1 / (mean sample time x %d layers x %d sequences)" % (
                   n_res, wl.num_layers, wl.num_layers, wl.batch))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": "decode steps/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+        # steps and ms_per_step describe what was timed (one layer of one sequence per
+        # step); the workload step is extrapolation_factor such samples
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(per_layer_seq * 1e3, 3),
+        "timed_s": round(sum(times), 3), "extrapolation_factor": factor,
+        "ms_per_workload_step_extrapolated": round(step_s * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded N(0,1) inputs)",
         "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.num_layers, "window": wl.window,

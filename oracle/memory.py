@@ -10,7 +10,7 @@ in FP8 KV Cache > How It Works).  positions = min(context, window) when a window
 set.
 
 Parity: pinned by tests/test_oracle_memory.py against the page's own table values
-(tests/golden/pages_memory_tables.json).
+(tests/golden/pages_figures.json).
 """
 
 ELEM_BYTES = {"f32": 4, "bf16": 2, "e4m3": 1}
