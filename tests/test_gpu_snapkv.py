@@ -10,17 +10,18 @@ window, 8 KV heads with planted heads, a ragged H2O batch whose first selection
 evicts (SnapKV's one-shot compression), n_obs of 32, 7 and 1, and the 32K-context
 FP8 batch at full size.
 
-Bars: the masses here sum the weights of n_obs queries (up to n_obs per head where a
-key dominates), so the decode step's 1e-4 absolute bar gains a relative term,
-|got - ref| <= 1e-4 + rho |ref|, on masses, tables and the selection's cut-off band.
-rho comes from the arithmetic of the logits:
-- bf16 caches: the logits are fp32 sums of exact bf16 products, with an error of a
-  few units in 2^-24 of a logit of magnitude up to ~20 (log2 units).  That is ~1e-6
-  relative on each weight; rho = 1e-5.
-- E4M3 caches: the queries are rounded to f16 (2^-11 relative), which moves a logit by
-  ~2^-12 sqrt(D) |q_d k_d| / sqrt(D), about 2.5e-4 for unit-variance inputs and a few
-  times that at worst; rho = 1e-3.
-Kept sets must be equal except near the cut-off.
+Bar: these masses sum the weights of n_obs queries and are then max-pooled, so they
+reach tens to hundreds (a vote is at most n_obs per head, a pooled in-block sum at most
+16 n_obs), where the decode step's masses stay below the number of heads.  The GPU
+computes them in float32, whose error is relative: a logit of magnitude |s| <= 32
+(log2 units) carries at most ~|s| 2^-23 of rounding, i.e. a relative weight error of
+<= 32 * 2^-23 * ln 2 = 2.6e-6, and summing up to 512 positive float32 terms adds a few
+2^-24 more.  So the decode bar gains a relative term, |got - ref| <= 1e-4 + RHO |ref|
+with RHO = 1e-5, for every storage format (the E4M3 path converts the bf16 queries to
+f16, which is exact in f16's normal range, and its keys' E4M3 values are exact in f16
+too).  Measured worst relative error: about 6e-7 for both formats.  The bar applies to
+masses, tables and the selection's cut-off band; kept sets must be equal except near
+the cut-off.
 """
 import dataclasses
 
@@ -36,11 +37,11 @@ from tests.test_gpu_parity import SMALL
 pytestmark = pytest.mark.gpu
 
 
-RHO = {"bf16": 1e-5, "e4m3": 1e-3}
+RHO = 1e-5
 
 
 def _snap_run(wl, n_obs, oseqs, steps):
-    rho = RHO[wl.kv_format]
+    rho = RHO
     run = harness.Run(wl, oracle_seqs=oseqs, kernel=kvs.KERNEL_TENSOR, obs_window=32)
     run.prefill()
     worst = run.prefill_score(n_obs, rel=rho)
