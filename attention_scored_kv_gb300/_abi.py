@@ -47,28 +47,35 @@ class Layout(ctypes.Structure):
                 ("reserved", ctypes.c_int32 * 2)]
 
 
+class Seqs(ctypes.Structure):
+    """kvs_seqs: a range (h_ids = d_ids = NULL) or a host + device list of ids."""
+    _fields_ = [("begin", ctypes.c_int32), ("count", ctypes.c_int32), ("h_ids", ctypes.c_void_p),
+                ("d_ids", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _I = ctypes.c_int32
+_S = Seqs
 _SIGS = {
     "kvs_config_init": (None, [ctypes.POINTER(Config)]),
     "kvs_validate_config": (_I, [ctypes.POINTER(Config), ctypes.c_char_p, ctypes.c_size_t]),
     "kvs_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config)]),
     "kvs_create": (_I, [ctypes.POINTER(Config), _P, ctypes.c_size_t, _P, ctypes.POINTER(_P)]),
     "kvs_destroy": (_I, [_P]),
-    "kvs_reset": (_I, [_P, _I, _I, _P]),
-    "kvs_append_kv": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
-    "kvs_decode_attend": (_I, [_P, _I, _I, _I, _P, _P, _P]),
-    "kvs_append_attend": (_I, [_P, _I, _I, _I, _P, _P, _P, _P, _P]),
-    "kvs_attend_blocks": (_I, [_P, _I, _I, _I, _P, _I, _P, _P, _P, _P]),
-    "kvs_decode_attend_static_scratch": (_I, [_P, _I, _I, _I, _P, _P, _P]),
-    "kvs_accumulate_scores": (_I, [_P, _I, _I, _P]),
-    "kvs_prefill_score": (_I, [_P, _I, _I, _I, _P, _I, _P]),
-    "kvs_select_blocks": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
-    "kvs_accumulate_select": (_I, [_P, _I, _I, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
-    "kvs_filter_blocks": (_I, [_P, _I, _I, _I, ctypes.c_double, _P, _I, _P, _P]),
+    "kvs_reset": (_I, [_P, _S, _P]),
+    "kvs_append_kv": (_I, [_P, _I, _S, _I, _P, _P, _P]),
+    "kvs_decode_attend": (_I, [_P, _I, _S, _P, _P, _P, _P]),
+    "kvs_append_attend": (_I, [_P, _I, _S, _P, _P, _P, _P, _P, _P]),
+    "kvs_attend_blocks": (_I, [_P, _I, _S, _P, _I, _P, _P, _P, _P]),
+    "kvs_decode_attend_static_scratch": (_I, [_P, _I, _S, _P, _P, _P, _P]),
+    "kvs_accumulate_scores": (_I, [_P, _S, _P]),
+    "kvs_prefill_score": (_I, [_P, _I, _S, _P, _I, _P]),
+    "kvs_select_blocks": (_I, [_P, _S, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
+    "kvs_accumulate_select": (_I, [_P, _S, _P, _I, _I, ctypes.c_uint32, _P, _I, _P, _P]),
+    "kvs_filter_blocks": (_I, [_P, _S, _I, ctypes.c_double, _P, _I, _P, _P]),
     "kvs_scores_snapshot_bytes": (ctypes.c_size_t, [_P, _I]),
-    "kvs_export_scores": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
-    "kvs_import_scores": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
+    "kvs_export_scores": (_I, [_P, _S, _P, ctypes.c_size_t, _P]),
+    "kvs_import_scores": (_I, [_P, _S, _P, ctypes.c_size_t, _P]),
     "kvs_state_bytes": (ctypes.c_size_t, [_P, _I]),
     "kvs_read_state": (_I, [_P, _I, _I, _P, ctypes.c_size_t, _P]),
     "kvs_get_layout": (_I, [_P, ctypes.POINTER(Layout)]),

@@ -9,8 +9,8 @@ namespace {
 
 constexpr int kBlocksPerCta = 16;     // 16 blocks x 16 positions = 256 threads
 
-__global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
-  const int s = seq_begin + blockIdx.y;
+__global__ void __launch_bounds__(256) accumulate_kernel(Dev d, SeqSel sel) {
+  const int s = sel.at(blockIdx.y);
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
   const int i = blockIdx.x * kBlocksPerCta + (threadIdx.x >> 4);
@@ -46,11 +46,11 @@ __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, int seq_begin) {
 
 }  // namespace
 
-cudaError_t launch_accumulate(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+cudaError_t launch_accumulate(const Dev& d, SeqSel sel, int n_seqs, int max_blocks_per_seq,
                               cudaStream_t st) {
   dim3 grid((max_blocks_per_seq + kBlocksPerCta - 1) / kBlocksPerCta, n_seqs);
   if (grid.x == 0) grid.x = 1;
-  accumulate_kernel<<<grid, 256, 0, st>>>(d, seq_begin);
+  accumulate_kernel<<<grid, 256, 0, st>>>(d, sel);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,7 @@ __device__ __forceinline__ int scan_flags(int flag, int32_t* warp_sums, int* tot
   return before + __popc(bal & ((1u << lane) - 1u));
 }
 
-__global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int seq_begin, const int32_t* k_per_seq,
+__global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, SeqSel sel, const int32_t* k_per_seq,
                                                                      int k_uniform, int kind, uint32_t flags,
                                                                      int32_t* keep_ids, int keep_capacity,
                                                                      int32_t* keep_count) {
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
   __shared__ uint64_t s_prefix;
   __shared__ int32_t s_take;
   const int lane_id = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
-  const int sl = blockIdx.y, s = seq_begin + sl, tid = threadIdx.x;
+  const int sl = blockIdx.y, s = sel.at(sl), tid = threadIdx.x;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
 
@@ -191,12 +191,12 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, int 
 
 int accumulate_select_max_blocks() { return kRankMax; }
 
-cudaError_t launch_accumulate_select(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+cudaError_t launch_accumulate_select(const Dev& d, SeqSel sel, int n_seqs, int max_blocks_per_seq,
                                      const int32_t* k_per_seq, int k_uniform, int score_kind, uint32_t flags,
                                      int32_t* keep_ids, int keep_capacity, int32_t* keep_count, cudaStream_t st) {
   dim3 grid((max_blocks_per_seq + kBlocksPerCta - 1) / kBlocksPerCta, n_seqs);
   if (grid.x == 0) grid.x = 1;
-  accumulate_select_kernel<<<grid, kThreads, 0, st>>>(d, seq_begin, k_per_seq, k_uniform, score_kind, flags,
+  accumulate_select_kernel<<<grid, kThreads, 0, st>>>(d, sel, k_per_seq, k_uniform, score_kind, flags,
                                                       keep_ids, keep_capacity, keep_count);
   return cudaGetLastError();
 }

@@ -17,10 +17,10 @@ constexpr int kWarps = 8;
 
 // grid (ceil(n_new / (kWarps/2)), n_seqs): two warps per new token, one for K, one for V.
 template <int KV, int IN>
-__global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, int seq_begin, int n_new,
+__global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, SeqSel sel, int n_new,
                                                                const void* k_in, const void* v_in) {
   const int s_local = blockIdx.y;
-  const int s = seq_begin + s_local;
+  const int s = sel.at(s_local);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t np_idx = (size_t)layer * d.max_seqs + s;
   const int64_t next0 = d.next_pos[np_idx];
@@ -68,10 +68,10 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, i
 
 // H2O: give every block that the new positions enter a page from the pool, in order,
 // and append it to the sequence's resident list.  One thread per sequence.
-__global__ void alloc_pages_kernel(Dev d, int layer, int seq_begin, int n_seqs, int n_new) {
+__global__ void alloc_pages_kernel(Dev d, int layer, SeqSel sel, int n_seqs, int n_new) {
   const int sl = blockIdx.x * blockDim.x + threadIdx.x;
   if (sl >= n_seqs) return;
-  const int s = seq_begin + sl;
+  const int s = sel.at(sl);
   const int64_t next0 = d.next_pos[(size_t)layer * d.max_seqs + s];
   const int64_t last = next0 + n_new - 1;
   if (n_new <= 0 || last >= d.max_positions) return;   // the append reports capacity
@@ -97,21 +97,21 @@ __global__ void alloc_pages_kernel(Dev d, int layer, int seq_begin, int n_seqs, 
 
 }  // namespace
 
-cudaError_t launch_alloc_pages(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+cudaError_t launch_alloc_pages(const Dev& d, int layer, SeqSel sel, int n_seqs, int n_new,
                                cudaStream_t st) {
-  alloc_pages_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(d, layer, seq_begin, n_seqs, n_new);
+  alloc_pages_kernel<<<(n_seqs + 127) / 128, 128, 0, st>>>(d, layer, sel, n_seqs, n_new);
   return cudaGetLastError();
 }
 
-cudaError_t launch_append(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+cudaError_t launch_append(const Dev& d, int layer, SeqSel sel, int n_seqs, int n_new,
                           const void* k, const void* v, cudaStream_t st) {
   dim3 grid((n_new + kWarps / 2 - 1) / (kWarps / 2), n_seqs);
   const int KV = d.kv_dtype, IN = d.in_dtype;
-  if (KV == KVS_E4M3 && IN == KVS_BF16) append_kernel<KVS_E4M3, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
-  else if (KV == KVS_E4M3 && IN == KVS_F32) append_kernel<KVS_E4M3, KVS_F32><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
-  else if (KV == KVS_BF16) append_kernel<KVS_BF16, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
-  else if (KV == KVS_F32 && IN == KVS_BF16) append_kernel<KVS_F32, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
-  else append_kernel<KVS_F32, KVS_F32><<<grid, kWarps * 32, 0, st>>>(d, layer, seq_begin, n_new, k, v);
+  if (KV == KVS_E4M3 && IN == KVS_BF16) append_kernel<KVS_E4M3, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, sel, n_new, k, v);
+  else if (KV == KVS_E4M3 && IN == KVS_F32) append_kernel<KVS_E4M3, KVS_F32><<<grid, kWarps * 32, 0, st>>>(d, layer, sel, n_new, k, v);
+  else if (KV == KVS_BF16) append_kernel<KVS_BF16, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, sel, n_new, k, v);
+  else if (KV == KVS_F32 && IN == KVS_BF16) append_kernel<KVS_F32, KVS_BF16><<<grid, kWarps * 32, 0, st>>>(d, layer, sel, n_new, k, v);
+  else append_kernel<KVS_F32, KVS_F32><<<grid, kWarps * 32, 0, st>>>(d, layer, sel, n_new, k, v);
   return cudaGetLastError();
 }
 

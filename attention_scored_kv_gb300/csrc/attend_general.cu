@@ -61,14 +61,15 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // scratch per sequence: logits [Hq][cap] (log2 domain), cap = entries capacity
 template <int KV, int IN>
-__global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int layer, int seq_begin,
-                                                                  const void* q, float* out, int cap) {
+__global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int layer, SeqSel sel,
+                                                                  const void* q, float* out, float* tok_out,
+                                                                  int cap) {
   extern __shared__ float sm[];
   float* qs = sm;                                  // [Hq][D]
   float* mh = qs + d.Hq * d.D;                     // [Hq] max
   float* lh = mh + d.Hq;                           // [Hq] sum
   float* red = lh + d.Hq;                          // [32]
-  const int sl = blockIdx.x, s = seq_begin + sl;
+  const int sl = blockIdx.x, s = sel.at(sl);
   const SeqBlocks sb = seq_blocks(d, layer, s);
   const int n = sb.n * kBlock;                     // entries incl. masked ones
   if (n == 0 || n > cap) {
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int lay
     int32_t slot;
     page = page_of(d, s, p, &slot);
     d.tok_mass[lay_slot + (size_t)page * kBlock + slot] = tau;
+    if (tok_out) tok_out[(size_t)sl * d.max_positions + p] = tau;
   }
   for (int i = threadIdx.x; i < sb.n; i += kThreads) {
     int32_t page;
@@ -169,8 +171,8 @@ __global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int lay
 
 size_t general_smem_bytes(int Hq, int D) { return ((size_t)Hq * D + 2 * Hq + 32) * sizeof(float); }
 
-cudaError_t launch_attend_general(const Dev& d, int layer, int seq_begin, int n_seqs,
-                                  const void* q, float* out, cudaStream_t st) {
+cudaError_t launch_attend_general(const Dev& d, int layer, SeqSel sel, int n_seqs,
+                                  const void* q, float* out, float* tok_out, cudaStream_t st) {
   const int cap = (int)(d.logit_scratch_elems / ((size_t)n_seqs * d.Hq));
   const size_t smem = general_smem_bytes(d.Hq, d.D);
   const int KV = d.kv_dtype, IN = d.in_dtype;
@@ -178,7 +180,7 @@ cudaError_t launch_attend_general(const Dev& d, int layer, int seq_begin, int n_
   do {                                                                                            \
     auto fn = attend_general_kernel<A, B>;                                                        \
     if (smem > 48 * 1024) cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem); \
-    fn<<<n_seqs, kThreads, smem, st>>>(d, layer, seq_begin, q, out, cap);                         \
+    fn<<<n_seqs, kThreads, smem, st>>>(d, layer, sel, q, out, tok_out, cap);                      \
   } while (0)
   if (KV == KVS_E4M3 && IN == KVS_BF16) KVS_LAUNCH(KVS_E4M3, KVS_BF16);
   else if (KV == KVS_E4M3) KVS_LAUNCH(KVS_E4M3, KVS_F32);

@@ -403,7 +403,8 @@ constexpr int kRingBytes = 144 * 1024;  // shared memory given to the TMA ring a
 constexpr int kMinStages = 2;
 
 struct Params {
-  int layer, seq_begin, n_seqs, cap;   // cap: blocks per CTA the buffers hold
+  int layer, n_seqs, cap;             // cap: blocks per CTA the buffers hold
+  SeqSel sel;                          // the launch's sequences: b-th is sel.at(b)
   int ns;                              // ring stages
   const void* q;                       // [n_seqs][HQ][D] bf16
   float* out;                          // [n_seqs][HQ][D]
@@ -425,6 +426,7 @@ struct Params {
   const int32_t* list_ids;
   const int32_t* list_count;
   int list_stride;
+  float* tok_out;                      // optional: entry masses at [b][position] too
 };
 
 // Page of block k of sequence s for a block list: the slot rule of the mode, or the
@@ -572,12 +574,12 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     if (c < P.cst[P.n_seqs]) {
       const int lo = P.cta_seq[c];          // one lookup (a search costs a chain of loads)
       wseq = lo;
-      int64_t nxt = d.next_pos[(size_t)P.layer * d.max_seqs + P.seq_begin + lo];
+      int64_t nxt = d.next_pos[(size_t)P.layer * d.max_seqs + P.sel.at(lo)];
       // fused append: attend over the state after the new position (the host checked the
       // capacity; a state that disagrees skips the append and reports it)
       const bool grow = P.fuse && nxt < d.max_positions;
       if (P.fuse && !grow && tid == 0) set_error(d, kErrCapacity);
-      sbw = seq_blocks_at(d, P.seq_begin + lo, grow ? nxt + 1 : nxt);
+      sbw = seq_blocks_at(d, P.sel.at(lo), grow ? nxt + 1 : nxt);
       if (P.list_ids) sbw.n = min(max(P.list_count[lo], 0), P.list_stride);
       const int cb = P.cst[lo + 1] - P.cst[lo], rk = c - P.cst[lo];
       const int qb = sbw.n / cb, rb = sbw.n % cb;
@@ -594,7 +596,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         const int b = b0 + lane;
         int nb = 0;
         if (b < P.n_seqs) {
-          SeqBlocks sb = seq_blocks(d, P.layer, P.seq_begin + b);
+          SeqBlocks sb = seq_blocks(d, P.layer, P.sel.at(b));
           if (P.list_ids) sb.n = min(max(P.list_count[b], 0), P.list_stride);
           seqb[b] = sb;
           nb = sb.n;
@@ -628,9 +630,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       int32_t page, k;
       if (P.list_ids) {
         k = P.list_ids[(size_t)cseq * P.list_stride + x0 + i];
-        page = list_block(d, P.seq_begin + cseq, &k);
+        page = list_block(d, P.sel.at(cseq), &k);
       } else {
-        k = block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+        k = block_at(d, P.sel.at(cseq), sbw, x0 + i, &page);
       }
       blk_id[i] = k;
       blk_page[i] = page;
@@ -647,9 +649,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       int32_t page, k;
       if (P.list_ids) {
         k = P.list_ids[(size_t)lo * P.list_stride + x - prefix[lo]];
-        page = list_block(d, P.seq_begin + lo, &k);
+        page = list_block(d, P.sel.at(lo), &k);
       } else {
-        k = block_at(d, P.seq_begin + lo, seqb[lo], x - prefix[lo], &page);
+        k = block_at(d, P.sel.at(lo), seqb[lo], x - prefix[lo], &page);
       }
       blk_id[i] = k;
       blk_page[i] = page;
@@ -664,7 +666,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     // A CTA of the whole plan with no block still read its sequence's next position:
     // it departs too, so that the last CTA to leave knows every reader is done.
     if (wseq >= 0 && tid == 0) {
-      const int s = P.seq_begin + wseq, cb = P.cst[wseq + 1] - P.cst[wseq];
+      const int s = P.sel.at(wseq), cb = P.cst[wseq + 1] - P.cst[wseq];
       if (atomicAdd(ctr_base + (size_t)s * kCounterInts + kDepartAt, 1) == cb - 1) {
         ctr_base[(size_t)s * kCounterInts] = 0;
         ctr_base[(size_t)s * kCounterInts + kDepartAt] = 0;
@@ -687,9 +689,9 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
         int32_t page;
         if (P.list_ids) {
           int32_t k = P.list_ids[(size_t)cseq * P.list_stride + x0 + i];
-          page = list_block(d, P.seq_begin + cseq, &k);
+          page = list_block(d, P.sel.at(cseq), &k);
         } else {
-          block_at(d, P.seq_begin + cseq, sbw, x0 + i, &page);
+          block_at(d, P.sel.at(cseq), sbw, x0 + i, &page);
         }
         ppage[i] = page;
       }
@@ -735,7 +737,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     if (early) {
       // publish the partial output rows once this CTA's consumers have written them
       named_sync(kBarOut, kPubThreads);
-      if (lane == 0) red_release_add(ctr_base + (size_t)(P.seq_begin + cseq) * kCounterInts, 1);
+      if (lane == 0) red_release_add(ctr_base + (size_t)(P.sel.at(cseq)) * kCounterInts, 1);
     }
   } else if (warp == kNormWarp) {
     // ============================================================== normaliser warp
@@ -744,7 +746,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       // as the append kernel does while the consumers already run the K pass; the
       // producer copies the newest block only after app_bar.  Every storing lane orders
       // its generic-proxy stores before those copies.
-      const int s = P.seq_begin + cseq;
+      const int s = P.sel.at(cseq);
       const int64_t pnew = sbw.next - 1;
       int32_t slot;
       const int32_t page = page_of(d, s, pnew, &slot);
@@ -773,7 +775,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       // wait (bounded) until every CTA of the sequence has published its statistics,
       // then lane h merges head h's records in record order.  Record k is the
       // sequence's k-th CTA: per head the running max m and l = sum exp2(s - m).
-      const int b = cseq, s = P.seq_begin + b;
+      const int b = cseq, s = P.sel.at(b);
       const int cb = P.cst[b + 1] - P.cst[b], cf = P.cst[b];
       const int S = sbw.n >= cb ? cb : sbw.n;
       int ok = 1;
@@ -854,7 +856,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     while (i0 < nblk) {
       int i1 = i0 + 1;
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
-      const int b = blk_seq[i0], s = P.seq_begin + b;
+      const int b = blk_seq[i0], s = P.sel.at(b);
       const SeqBlocks sb = seqb[b];
 
       // Q fragments of head kvh*8 + g (B operand of QK^T)
@@ -1011,7 +1013,7 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
     while (i0 < nblk) {
       int i1 = i0 + 1;
       while (i1 < nblk && blk_seq[i1] == blk_seq[i0]) ++i1;
-      const int b = blk_seq[i0], s = P.seq_begin + b;
+      const int b = blk_seq[i0], s = P.sel.at(b);
       const SeqBlocks sb = seqb[b];
       int cf, S;                                   // the sequence's CTAs: cf .. cf + S - 1
       if (P.whole) {
@@ -1128,6 +1130,13 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
               if (p0 + 1 >= sb.lo && p0 + 1 < sb.next) dst[1] = tau.y;
               if (p0 + 2 >= sb.lo && p0 + 2 < sb.next) dst[2] = tau.z;
               if (p0 + 3 >= sb.lo && p0 + 3 < sb.next) dst[3] = tau.w;
+            }
+            if (P.tok_out) {                     // the caller's copy, by absolute position
+              float* to = P.tok_out + (size_t)b * d.max_positions + p0;
+              if (p0 >= sb.lo && p0 < sb.next) to[0] = tau.x;
+              if (p0 + 1 >= sb.lo && p0 + 1 < sb.next) to[1] = tau.y;
+              if (p0 + 2 >= sb.lo && p0 + 2 < sb.next) to[2] = tau.z;
+              if (p0 + 3 >= sb.lo && p0 + 3 < sb.next) to[3] = tau.w;
             }
             if (c4 == 0)
               d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
@@ -1342,14 +1351,15 @@ int tc_cap(int64_t T_bound, int grid) { return (int)((T_bound + grid - 1) / grid
 // possible or its buffers do not fit.  opt.list_ids non-null: attend over the listed
 // blocks only (bounds then bound the list lengths).
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                             int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
+                             SeqSel sel, int n_seqs, const void* q, float* out, const int32_t* bounds,
                              int grid, const AttendOpts& opt, cudaStream_t st) {
   const void* k_new = opt.k_new;
   const void* v_new = opt.v_new;
   Params P;
   P.layer = layer;
-  P.seq_begin = seq_begin;
+  P.sel = sel;
   P.n_seqs = n_seqs;
+  P.tok_out = opt.tok_out;
   int64_t T_bound = 0;
   for (int b = 0; b < n_seqs; ++b) T_bound += bounds[b];
   const int cap0 = tc_cap(T_bound, grid) < 1 ? 1 : tc_cap(T_bound, grid);
@@ -1466,15 +1476,16 @@ cudaError_t static_scratch_address(void** out) {
 // cudaErrorNotSupported if its logits do not fit in shared memory (that case needs the
 // workspace's logit scratch).
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                                    int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
-                                    int grid, cudaStream_t st) {
+                                    SeqSel sel, int n_seqs, const void* q, float* out, float* tok_out,
+                                    const int32_t* bounds, int grid, cudaStream_t st) {
   size_t ml_off = 0;
   const size_t need = static_scratch_need(d, n_seqs, grid, &ml_off);
   if (need > kStaticScratchBytes) return cudaErrorInvalidValue;
   Params P;
   P.layer = layer;
-  P.seq_begin = seq_begin;
+  P.sel = sel;
   P.n_seqs = n_seqs;
+  P.tok_out = tok_out;
   int64_t T_bound = 0;
   for (int b = 0; b < n_seqs; ++b) T_bound += bounds[b];
   const int cap0 = tc_cap(T_bound, grid) < 1 ? 1 : tc_cap(T_bound, grid);

@@ -21,14 +21,14 @@ namespace kvs {
 bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window, int mode);
 cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                             int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
+                             SeqSel sel, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
                              const AttendOpts& opt, cudaStream_t st);
 int tc_grid(int kv_dtype, int Hkv, int sm_count);
 size_t static_scratch_limit();
 size_t static_scratch_need(const Dev& d, int n_seqs, int grid, size_t* ml_offset);
 cudaError_t launch_attend_tc_static(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
-                                    int seq_begin, int n_seqs, const void* q, float* out, const int32_t* bounds,
-                                    int grid, cudaStream_t st);
+                                    SeqSel sel, int n_seqs, const void* q, float* out, float* tok_out,
+                                    const int32_t* bounds, int grid, cudaStream_t st);
 }  // namespace kvs
 
 using namespace kvs;
@@ -203,6 +203,8 @@ struct kvs_ctx {
   std::vector<int64_t> frontier;    // [max_seqs] max over layers of next (pages allocated below it)
   std::vector<int64_t> h2o_bound;   // [max_seqs] bound on resident blocks (H2O)
   std::vector<int32_t> bounds;      // per-launch scratch: block bound of each sequence
+  std::vector<int32_t> sids;        // per-call scratch: the call's sequence ids, in order
+  std::vector<uint8_t> seen;        // per-call scratch: repeated-id check [max_seqs]
   std::vector<CUtensorMap> maps;    // [L][2]
   std::string err;
 };
@@ -226,11 +228,37 @@ kvs_status cuda_ok(kvs_ctx* ctx, cudaError_t e, const char* what) {
   return fail(ctx, KVS_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-kvs_status check_range(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs) {
-  if (n_seqs < 1 || seq_begin < 0 || (int64_t)seq_begin + n_seqs > ctx->cfg.max_seqs)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence range [%d, %d) outside [0, %d)", seq_begin,
-                seq_begin + n_seqs, ctx->cfg.max_seqs);
+// Check the sequences of a call and put their ids, in call order, in ctx->sids.
+kvs_status check_seqs(kvs_ctx* ctx, const kvs_seqs& q) {
+  const int B = ctx->cfg.max_seqs;
+  if (q.count < 1 || q.count > B) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence count %d outside [1, %d]", q.count, B);
+  ctx->sids.resize((size_t)q.count);
+  if (!q.h_ids && !q.d_ids) {
+    if (q.begin < 0 || (int64_t)q.begin + q.count > B)
+      return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence range [%d, %d) outside [0, %d)", q.begin,
+                  q.begin + q.count, B);
+    for (int i = 0; i < q.count; ++i) ctx->sids[i] = q.begin + i;
+    return KVS_OK;
+  }
+  if (!q.h_ids || !q.d_ids)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "a sequence list needs both its host and its device copy");
+  ctx->seen.assign((size_t)B, 0);
+  for (int i = 0; i < q.count; ++i) {
+    const int32_t s = q.h_ids[i];
+    if (s < 0 || s >= B) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence id %d outside [0, %d)", s, B);
+    if (ctx->seen[s]) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence id %d listed twice", s);
+    ctx->seen[s] = 1;
+    ctx->sids[i] = s;
+  }
   return KVS_OK;
+}
+
+// The kernels' view of the call's sequences.
+SeqSel sel_of(const kvs_seqs& q) {
+  SeqSel r;
+  r.begin = q.d_ids ? 0 : q.begin;
+  r.ids = q.d_ids;
+  return r;
 }
 
 int64_t seq_block_bound(const kvs_ctx* ctx, int s) {
@@ -267,24 +295,35 @@ int snapshot_sections(const kvs_ctx* ctx, int seq_begin, int n, void* ptr[11], s
 
 size_t round256(size_t b) { return (b + 255) & ~(size_t)255; }
 
-kvs_status snapshot_copy(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* buf, size_t buf_bytes, bool out,
+// A snapshot holds one section per table (snapshot_sections order, each 256-byte
+// aligned) with the rows of the call's sequences in call order.  A range's rows are
+// contiguous in both places (one copy per table); a list's are copied row by row.
+kvs_status snapshot_copy(kvs_ctx* ctx, const kvs_seqs& seqs, void* buf, size_t buf_bytes, bool out,
                          kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  const size_t need = kvs_scores_snapshot_bytes(ctx, n_seqs);
+  const int n = seqs.count;
+  const size_t need = kvs_scores_snapshot_bytes(ctx, n);
   if (!buf || buf_bytes < need) return fail(ctx, KVS_ERR_CAPACITY, "snapshot needs %zu bytes", need);
-  void* ptr[11];
-  size_t bytes[11];
-  const int ns = snapshot_sections(ctx, seq_begin, n_seqs, ptr, bytes);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(buf);
+  const bool list = seqs.h_ids != nullptr;
+  void* ptr[11];
+  size_t bytes[11];
+  const int ns = snapshot_sections(ctx, list ? 0 : seqs.begin, n, ptr, bytes);
+  void* row0[11];
+  size_t rowb[11];
+  snapshot_sections(ctx, 0, 1, row0, rowb);                  // one sequence's row of each table
   size_t off = 0;
   for (int i = 0; i < ns; ++i) {
-    if (bytes[i]) {
-      void* dst = out ? static_cast<void*>(b + off) : ptr[i];
-      const void* src = out ? ptr[i] : static_cast<const void*>(b + off);
-      st = cuda_ok(ctx, cudaMemcpyAsync(dst, src, bytes[i], cudaMemcpyDefault, cs), out ? "export scores" : "import scores");
+    for (int r = 0; r < (list ? n : 1) && bytes[i]; ++r) {
+      const size_t len = list ? rowb[i] : bytes[i];
+      uint8_t* dev = static_cast<uint8_t*>(list ? row0[i] : ptr[i]) + (list ? (size_t)ctx->sids[r] * rowb[i] : 0);
+      uint8_t* host = b + off + (list ? (size_t)r * rowb[i] : 0);
+      void* dst = out ? static_cast<void*>(host) : static_cast<void*>(dev);
+      const void* src = out ? static_cast<const void*>(dev) : static_cast<const void*>(host);
+      st = cuda_ok(ctx, cudaMemcpyAsync(dst, src, len, cudaMemcpyDefault, cs), out ? "export scores" : "import scores");
       if (st != KVS_OK) return st;
     }
     off += round256(bytes[i]);
@@ -292,6 +331,72 @@ kvs_status snapshot_copy(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* 
   return KVS_OK;
 }
 
+}  // namespace
+
+namespace {
+// Checks shared by the attend entry points: q and out present and 16-byte aligned, the
+// optional token-mass output 4-byte aligned.
+kvs_status check_attend_buffers(kvs_ctx* ctx, const void* d_q, const float* d_out, const float* d_tok) {
+  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
+  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  if (reinterpret_cast<uintptr_t>(d_tok) & 3)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "the token-mass output must be 4-byte aligned");
+  return KVS_OK;
+}
+
+// Per sequence of the call: not empty in `layer`; its block bound into ctx->bounds.
+kvs_status attend_bounds(kvs_ctx* ctx, int32_t layer) {
+  const int B = ctx->cfg.max_seqs;
+  ctx->bounds.resize(ctx->sids.size());
+  for (size_t i = 0; i < ctx->sids.size(); ++i) {
+    const int32_t s = ctx->sids[i];
+    if (ctx->next[(size_t)layer * B + s] == 0)
+      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
+    ctx->bounds[i] = (int32_t)seq_block_bound(ctx, s);
+  }
+  return KVS_OK;
+}
+}  // namespace
+
+namespace {
+// accumulate checks: the layers of every sequence of the call agree on next_position;
+// returns the largest block bound through *maxb.
+kvs_status accumulate_bounds(kvs_ctx* ctx, int64_t* maxb) {
+  const int B = ctx->cfg.max_seqs;
+  *maxb = 1;
+  for (const int32_t s : ctx->sids) {
+    const int64_t n0 = ctx->next[s];
+    for (int l = 1; l < ctx->cfg.num_layers; ++l)
+      if (ctx->next[(size_t)l * B + s] != n0)
+        return fail(ctx, KVS_ERR_STATE, "sequence %d: layers disagree on next_position", s);
+    *maxb = std::max(*maxb, seq_block_bound(ctx, s));
+  }
+  return KVS_OK;
+}
+
+kvs_status check_select_args(kvs_ctx* ctx, int32_t score_kind, uint32_t flags, const int32_t* d_k_per_seq,
+                             int32_t k_uniform, const int32_t* d_keep_ids, int32_t keep_capacity,
+                             const int32_t* d_keep_count) {
+  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
+  if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
+  if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
+  if (!d_k_per_seq && k_uniform < 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "k must be >= 0");
+  if (!d_keep_ids || !d_keep_count || keep_capacity < 1)
+    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "keep buffers missing or keep_capacity < 1");
+  return KVS_OK;
+}
+
+// After an eviction with a uniform k: kept <= max(k, protected blocks), protected <=
+// sink blocks + recent blocks + 1.
+void shrink_h2o_bounds(kvs_ctx* ctx, uint32_t flags, const int32_t* d_k_per_seq, int32_t k_uniform) {
+  if (!(flags & KVS_SELECT_APPLY) || d_k_per_seq) return;
+  const int64_t prot = cdiv64(ctx->cfg.h2o_sink_tokens, kBlock) + cdiv64(ctx->plan.recent_tokens, kBlock) + 1;
+  const int64_t kept = std::max<int64_t>(k_uniform, (flags & KVS_SELECT_PROTECT) ? prot : 0);
+  for (const int32_t s : ctx->sids) ctx->h2o_bound[s] = std::min(ctx->h2o_bound[s], kept);
+}
 }  // namespace
 
 extern "C" {
@@ -438,13 +543,13 @@ kvs_status kvs_destroy(kvs_ctx* ctx) {
   return KVS_OK;
 }
 
-kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream) {
+kvs_status kvs_reset(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  st = cuda_ok(ctx, launch_reset(ctx->dev, seq_begin, n_seqs, reinterpret_cast<cudaStream_t>(stream)), "reset");
+  st = cuda_ok(ctx, launch_reset(ctx->dev, sel_of(seqs), seqs.count, reinterpret_cast<cudaStream_t>(stream)), "reset");
   if (st != KVS_OK) return st;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+  for (const int32_t s : ctx->sids) {
     for (int l = 0; l < ctx->cfg.num_layers; ++l) ctx->next[(size_t)l * ctx->cfg.max_seqs + s] = 0;
     ctx->frontier[s] = 0;
     ctx->h2o_bound[s] = 0;
@@ -452,17 +557,17 @@ kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream
   return KVS_OK;
 }
 
-kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, int32_t n_new,
-                         const void* d_k, const void* d_v, kvs_stream_t stream) {
+kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, int32_t n_new, const void* d_k,
+                         const void* d_v, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   if (n_new < 1) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "n_new must be >= 1");
   if (!d_k || !d_v) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL K or V");
   const int B = ctx->cfg.max_seqs;
   bool lead = false;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+  for (const int32_t s : ctx->sids) {
     const int64_t nx = ctx->next[(size_t)layer * B + s];
     if (nx + n_new > ctx->cfg.max_positions)
       return fail(ctx, KVS_ERR_CAPACITY, "sequence %d: position %lld + %d exceeds max_positions %d", s,
@@ -471,12 +576,12 @@ kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t
   }
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (ctx->plan.mode == KVS_MODE_H2O && lead) {
-    st = cuda_ok(ctx, launch_alloc_pages(ctx->dev, layer, seq_begin, n_seqs, n_new, cs), "page allocation");
+    st = cuda_ok(ctx, launch_alloc_pages(ctx->dev, layer, sel_of(seqs), seqs.count, n_new, cs), "page allocation");
     if (st != KVS_OK) return st;
   }
-  st = cuda_ok(ctx, launch_append(ctx->dev, layer, seq_begin, n_seqs, n_new, d_k, d_v, cs), "append");
+  st = cuda_ok(ctx, launch_append(ctx->dev, layer, sel_of(seqs), seqs.count, n_new, d_k, d_v, cs), "append");
   if (st != KVS_OK) return st;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+  for (const int32_t s : ctx->sids) {
     int64_t& nx = ctx->next[(size_t)layer * B + s];
     nx += n_new;
     if (nx > ctx->frontier[s]) {
@@ -488,61 +593,60 @@ kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t
   return KVS_OK;
 }
 
-kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_q,
-                             float* d_out, kvs_stream_t stream) {
+
+kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q, float* d_out,
+                             float* d_tok_mass_opt, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
-  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
-  const int B = ctx->cfg.max_seqs;
-  ctx->bounds.resize((size_t)n_seqs);
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
-    if (ctx->next[(size_t)layer * B + s] == 0)
-      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
-    ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
-  }
+  st = check_attend_buffers(ctx, d_q, d_out, d_tok_mass_opt);
+  if (st != KVS_OK) return st;
+  st = attend_bounds(ctx, layer);
+  if (st != KVS_OK) return st;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (ctx->kernel == KVS_KERNEL_TENSOR) {
-    return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
-                                         n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, AttendOpts{}, cs),
+    AttendOpts opt;
+    opt.tok_out = d_tok_mass_opt;
+    return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
+                                         seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt, cs),
                    "tensor-core attend");
   }
-  return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, seq_begin, n_seqs, d_q, d_out, cs), "attend");
+  return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, sel_of(seqs), seqs.count, d_q, d_out, d_tok_mass_opt, cs),
+                 "attend");
 }
 
-kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_k,
-                             const void* d_v, const void* d_q, float* d_out, kvs_stream_t stream) {
+kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_k, const void* d_v,
+                             const void* d_q, float* d_out, float* d_tok_mass_opt, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   if (!d_k || !d_v) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL K or V");
-  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
-  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  st = check_attend_buffers(ctx, d_q, d_out, d_tok_mass_opt);
+  if (st != KVS_OK) return st;
   if (ctx->kernel == KVS_KERNEL_TENSOR && ctx->plan.mode != KVS_MODE_H2O) {
     const int B = ctx->cfg.max_seqs;
-    ctx->bounds.resize((size_t)n_seqs);
-    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+    ctx->bounds.resize(ctx->sids.size());
+    for (size_t i = 0; i < ctx->sids.size(); ++i) {
+      const int32_t s = ctx->sids[i];
       const int64_t nx = ctx->next[(size_t)layer * B + s];
       if (nx + 1 > ctx->cfg.max_positions)
         return fail(ctx, KVS_ERR_CAPACITY, "sequence %d: position %lld + 1 exceeds max_positions %d", s,
                     (long long)nx, ctx->cfg.max_positions);
-      ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
+      ctx->bounds[i] = (int32_t)seq_block_bound(ctx, s);
     }
     AttendOpts opt;
     opt.k_new = d_k;
     opt.v_new = d_v;
+    opt.tok_out = d_tok_mass_opt;
     const cudaError_t e = launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
-                                           seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
+                                           sel_of(seqs), seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
                                            reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaErrorNotSupported) {
       st = cuda_ok(ctx, e, "tensor-core append + attend");
       if (st != KVS_OK) return st;
-      for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {   // the same shadow update as an append
+      for (const int32_t s : ctx->sids) {          // the same shadow update as an append
         int64_t& nx = ctx->next[(size_t)layer * B + s];
         nx += 1;
         if (nx > ctx->frontier[s]) {
@@ -554,47 +658,42 @@ kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
     }
   }
   // no single-launch form for this context or launch: the two steps, same results
-  st = kvs_append_kv(ctx, layer, seq_begin, n_seqs, 1, d_k, d_v, stream);
+  st = kvs_append_kv(ctx, layer, seqs, 1, d_k, d_v, stream);
   if (st != KVS_OK) return st;
-  return kvs_decode_attend(ctx, layer, seq_begin, n_seqs, d_q, d_out, stream);
+  return kvs_decode_attend(ctx, layer, seqs, d_q, d_out, d_tok_mass_opt, stream);
 }
 
-kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                             const int32_t* d_block_ids, int32_t ids_stride, const int32_t* d_block_count,
-                             const void* d_q, float* d_out, kvs_stream_t stream) {
+kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const int32_t* d_block_ids,
+                             int32_t ids_stride, const int32_t* d_block_count, const void* d_q, float* d_out,
+                             kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   if (!d_block_ids || !d_block_count || ids_stride < 1)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "block list missing or ids_stride < 1");
-  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
-  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  st = check_attend_buffers(ctx, d_q, d_out, nullptr);
+  if (st != KVS_OK) return st;
   if (ctx->kernel != KVS_KERNEL_TENSOR)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the block-list attend runs on the tensor-core attend only");
-  const int B = ctx->cfg.max_seqs;
-  ctx->bounds.resize((size_t)n_seqs);
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
-    if (ctx->next[(size_t)layer * B + s] == 0)
-      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
-    ctx->bounds[s - seq_begin] = (int32_t)std::min<int64_t>(ids_stride, seq_block_bound(ctx, s));
-  }
+  st = attend_bounds(ctx, layer);
+  if (st != KVS_OK) return st;
+  for (auto& b : ctx->bounds) b = std::min<int32_t>(ids_stride, b);
   AttendOpts opt;
   opt.list_ids = d_block_ids;
   opt.list_count = d_block_count;
   opt.list_stride = ids_stride;
-  return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, seq_begin,
-                                       n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
+  return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
+                                       seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
                                        reinterpret_cast<cudaStream_t>(stream)),
                  "tensor-core block-list attend");
 }
 
-kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs, const void* d_q_obs,
-                             int32_t n_obs, kvs_stream_t stream) {
+kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q_obs, int32_t n_obs,
+                             kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   if (ctx->cfg.obs_window == 0)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "prefill scoring is off: create the context with obs_window > 0");
@@ -604,7 +703,7 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q_obs must be a 16-byte aligned device pointer");
   const int B = ctx->cfg.max_seqs;
   int64_t maxb = 1;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
+  for (const int32_t s : ctx->sids) {
     const int64_t nx = ctx->next[(size_t)layer * B + s];
     if (nx < n_obs)
       return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "sequence %d holds %lld entries in layer %d, fewer than n_obs", s,
@@ -616,144 +715,107 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int
   maxb = std::min<int64_t>(maxb, ctx->plan.ps_bound);
   // chunk size: the largest (fewest CTAs, least fixed cost per block) unless the launch
   // would then leave SMs idle: two CTAs fit an SM
-  const int64_t units = maxb * n_seqs * ctx->cfg.num_kv_heads, slots = 2 * (int64_t)ctx->sm_count;
+  const int64_t units = maxb * seqs.count * ctx->cfg.num_kv_heads, slots = 2 * (int64_t)ctx->sm_count;
   const int cb = units >= (int64_t)kPrefillChunkMax * slots
                      ? kPrefillChunkMax
                      : (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, slots)));
   const int chunks = (int)cdiv64(maxb, cb);
-  return cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, seq_begin, n_seqs, d_q_obs, n_obs, cb, chunks,
+  return cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, sel_of(seqs), seqs.count, d_q_obs, n_obs, cb, chunks,
                                            reinterpret_cast<cudaStream_t>(stream)),
                  "prefill score");
 }
 
-kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                                            const void* d_q, float* d_out, kvs_stream_t stream) {
+kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q, float* d_out,
+                                            float* d_tok_mass_opt, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  if (!d_q || !d_out) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL q or out");
-  if ((reinterpret_cast<uintptr_t>(d_q) | reinterpret_cast<uintptr_t>(d_out)) & 15)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q and out must be 16-byte aligned");
+  st = check_attend_buffers(ctx, d_q, d_out, d_tok_mass_opt);
+  if (st != KVS_OK) return st;
   if (ctx->kernel != KVS_KERNEL_TENSOR)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the library-owned exchange area serves the tensor-core attend only");
-  const int B = ctx->cfg.max_seqs;
-  ctx->bounds.resize((size_t)n_seqs);
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
-    if (ctx->next[(size_t)layer * B + s] == 0)
-      return fail(ctx, KVS_ERR_EMPTY_CACHE, "sequence %d has no entry in layer %d (all-masked row)", s, layer);
-    ctx->bounds[s - seq_begin] = (int32_t)seq_block_bound(ctx, s);
-  }
+  st = attend_bounds(ctx, layer);
+  if (st != KVS_OK) return st;
   size_t off = 0;
-  const size_t need = static_scratch_need(ctx->dev, n_seqs, ctx->grid, &off);
+  const size_t need = static_scratch_need(ctx->dev, seqs.count, ctx->grid, &off);
   if (need > static_scratch_limit())
     return fail(ctx, KVS_ERR_CAPACITY, "this launch needs %zu bytes of exchange area; the library array holds %zu",
                 need, static_scratch_limit());
   const cudaError_t e = launch_attend_tc_static(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer,
-                                                seq_begin, n_seqs, d_q, d_out, ctx->bounds.data(), ctx->grid,
-                                                reinterpret_cast<cudaStream_t>(stream));
+                                                sel_of(seqs), seqs.count, d_q, d_out, d_tok_mass_opt,
+                                                ctx->bounds.data(), ctx->grid, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported)
     return fail(ctx, KVS_ERR_UNSUPPORTED, "the logits of this launch do not fit in shared memory");
   return cuda_ok(ctx, e, "tensor-core attend (library exchange area)");
 }
 
-kvs_status kvs_accumulate_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream) {
+
+kvs_status kvs_accumulate_scores(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  const int B = ctx->cfg.max_seqs;
   int64_t maxb = 1;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
-    const int64_t n0 = ctx->next[s];
-    for (int l = 1; l < ctx->cfg.num_layers; ++l)
-      if (ctx->next[(size_t)l * B + s] != n0)
-        return fail(ctx, KVS_ERR_STATE, "sequence %d: layers disagree on next_position", s);
-    maxb = std::max(maxb, seq_block_bound(ctx, s));
-  }
-  return cuda_ok(ctx, launch_accumulate(ctx->dev, seq_begin, n_seqs, (int)maxb, reinterpret_cast<cudaStream_t>(stream)),
+  st = accumulate_bounds(ctx, &maxb);
+  if (st != KVS_OK) return st;
+  return cuda_ok(ctx, launch_accumulate(ctx->dev, sel_of(seqs), seqs.count, (int)maxb,
+                                        reinterpret_cast<cudaStream_t>(stream)),
                  "accumulate");
 }
 
-kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const int32_t* d_k_per_seq,
-                             int32_t k_uniform, int32_t score_kind, uint32_t flags, int32_t* d_keep_ids,
-                             int32_t keep_capacity, int32_t* d_keep_count, kvs_stream_t stream) {
+kvs_status kvs_select_blocks(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform,
+                             int32_t score_kind, uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
+                             int32_t* d_keep_count, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
-  if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
-  if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
-  if (!d_k_per_seq && k_uniform < 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "k must be >= 0");
-  if (!d_keep_ids || !d_keep_count || keep_capacity < 1)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "keep buffers missing or keep_capacity < 1");
-  st = cuda_ok(ctx, launch_select(ctx->dev, seq_begin, n_seqs, d_k_per_seq, k_uniform, score_kind, flags, d_keep_ids,
-                                  keep_capacity, d_keep_count, reinterpret_cast<cudaStream_t>(stream)),
+  st = check_select_args(ctx, score_kind, flags, d_k_per_seq, k_uniform, d_keep_ids, keep_capacity, d_keep_count);
+  if (st != KVS_OK) return st;
+  st = cuda_ok(ctx, launch_select(ctx->dev, sel_of(seqs), seqs.count, d_k_per_seq, k_uniform, score_kind, flags,
+                                  d_keep_ids, keep_capacity, d_keep_count, reinterpret_cast<cudaStream_t>(stream)),
                "select");
   if (st != KVS_OK) return st;
-  if ((flags & KVS_SELECT_APPLY) && !d_k_per_seq) {
-    // kept <= max(k, protected blocks); protected <= sink blocks + recent blocks + 1
-    const int64_t prot = cdiv64(ctx->cfg.h2o_sink_tokens, kBlock) + cdiv64(ctx->plan.recent_tokens, kBlock) + 1;
-    const int64_t kept = std::max<int64_t>(k_uniform, (flags & KVS_SELECT_PROTECT) ? prot : 0);
-    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) ctx->h2o_bound[s] = std::min(ctx->h2o_bound[s], kept);
-  }
+  shrink_h2o_bounds(ctx, flags, d_k_per_seq, k_uniform);
   return KVS_OK;
 }
 
-kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const int32_t* d_k_per_seq,
-                                 int32_t k_uniform, int32_t score_kind, uint32_t flags, int32_t* d_keep_ids,
-                                 int32_t keep_capacity, int32_t* d_keep_count, kvs_stream_t stream) {
+kvs_status kvs_accumulate_select(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform,
+                                 int32_t score_kind, uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
+                                 int32_t* d_keep_count, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
-  if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
-  if (flags & ~(KVS_SELECT_PROTECT | KVS_SELECT_APPLY)) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "unknown flags");
-  if ((flags & KVS_SELECT_APPLY) && ctx->plan.mode != KVS_MODE_H2O)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "eviction (KVS_SELECT_APPLY) needs the H2O mode");
-  if (!d_k_per_seq && k_uniform < 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "k must be >= 0");
-  if (!d_keep_ids || !d_keep_count || keep_capacity < 1)
-    return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "keep buffers missing or keep_capacity < 1");
-  const int B = ctx->cfg.max_seqs;
+  st = check_select_args(ctx, score_kind, flags, d_k_per_seq, k_uniform, d_keep_ids, keep_capacity, d_keep_count);
+  if (st != KVS_OK) return st;
   int64_t maxb = 1;
-  for (int s = seq_begin; s < seq_begin + n_seqs; ++s) {
-    const int64_t n0 = ctx->next[s];
-    for (int l = 1; l < ctx->cfg.num_layers; ++l)
-      if (ctx->next[(size_t)l * B + s] != n0)
-        return fail(ctx, KVS_ERR_STATE, "sequence %d: layers disagree on next_position", s);
-    maxb = std::max(maxb, seq_block_bound(ctx, s));
-  }
+  st = accumulate_bounds(ctx, &maxb);
+  if (st != KVS_OK) return st;
   if (maxb > accumulate_select_max_blocks()) {   // long sequences: the two kernels
-    st = kvs_accumulate_scores(ctx, seq_begin, n_seqs, stream);
+    st = kvs_accumulate_scores(ctx, seqs, stream);
     if (st != KVS_OK) return st;
-    return kvs_select_blocks(ctx, seq_begin, n_seqs, d_k_per_seq, k_uniform, score_kind, flags, d_keep_ids,
-                             keep_capacity, d_keep_count, stream);
+    return kvs_select_blocks(ctx, seqs, d_k_per_seq, k_uniform, score_kind, flags, d_keep_ids, keep_capacity,
+                             d_keep_count, stream);
   }
-  st = cuda_ok(ctx, launch_accumulate_select(ctx->dev, seq_begin, n_seqs, (int)maxb, d_k_per_seq, k_uniform, score_kind, flags,
-                                             d_keep_ids, keep_capacity, d_keep_count,
+  st = cuda_ok(ctx, launch_accumulate_select(ctx->dev, sel_of(seqs), seqs.count, (int)maxb, d_k_per_seq, k_uniform,
+                                             score_kind, flags, d_keep_ids, keep_capacity, d_keep_count,
                                              reinterpret_cast<cudaStream_t>(stream)),
                "accumulate + select");
   if (st != KVS_OK) return st;
-  if ((flags & KVS_SELECT_APPLY) && !d_k_per_seq) {   // as kvs_select_blocks
-    const int64_t prot = cdiv64(ctx->cfg.h2o_sink_tokens, kBlock) + cdiv64(ctx->plan.recent_tokens, kBlock) + 1;
-    const int64_t kept = std::max<int64_t>(k_uniform, (flags & KVS_SELECT_PROTECT) ? prot : 0);
-    for (int s = seq_begin; s < seq_begin + n_seqs; ++s) ctx->h2o_bound[s] = std::min(ctx->h2o_bound[s], kept);
-  }
+  shrink_h2o_bounds(ctx, flags, d_k_per_seq, k_uniform);
   return KVS_OK;
 }
 
-kvs_status kvs_filter_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, int32_t score_kind, double theta,
-                             int32_t* d_ids, int32_t capacity, int32_t* d_count, kvs_stream_t stream) {
+kvs_status kvs_filter_blocks(kvs_ctx* ctx, kvs_seqs seqs, int32_t score_kind, double theta, int32_t* d_ids,
+                             int32_t capacity, int32_t* d_count, kvs_stream_t stream) {
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
-  kvs_status st = check_range(ctx, seq_begin, n_seqs);
+  kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   if (score_kind < KVS_SCORE_CUMULATIVE || score_kind > KVS_SCORE_TOVA)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "score_kind must be CUMULATIVE, EMA, TOKEN_SUM or TOVA");
   if (theta != theta) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "theta is NaN");
   if (!d_ids || !d_count || capacity < 1)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "output buffers missing or capacity < 1");
-  return cuda_ok(ctx, launch_filter(ctx->dev, seq_begin, n_seqs, score_kind, theta, d_ids, capacity, d_count,
+  return cuda_ok(ctx, launch_filter(ctx->dev, sel_of(seqs), seqs.count, score_kind, theta, d_ids, capacity, d_count,
                                     reinterpret_cast<cudaStream_t>(stream)),
                  "filter");
 }
@@ -768,14 +830,12 @@ size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs) {
   return total;
 }
 
-kvs_status kvs_export_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* dst, size_t dst_bytes,
-                             kvs_stream_t stream) {
-  return snapshot_copy(ctx, seq_begin, n_seqs, dst, dst_bytes, true, stream);
+kvs_status kvs_export_scores(kvs_ctx* ctx, kvs_seqs seqs, void* dst, size_t dst_bytes, kvs_stream_t stream) {
+  return snapshot_copy(ctx, seqs, dst, dst_bytes, true, stream);
 }
 
-kvs_status kvs_import_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const void* src, size_t src_bytes,
-                             kvs_stream_t stream) {
-  return snapshot_copy(ctx, seq_begin, n_seqs, const_cast<void*>(src), src_bytes, false, stream);
+kvs_status kvs_import_scores(kvs_ctx* ctx, kvs_seqs seqs, const void* src, size_t src_bytes, kvs_stream_t stream) {
+  return snapshot_copy(ctx, seqs, const_cast<void*>(src), src_bytes, false, stream);
 }
 
 size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {

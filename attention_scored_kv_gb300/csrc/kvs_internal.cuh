@@ -49,6 +49,14 @@ constexpr int kCounterInts = 96;
 constexpr int kDepartAt = 32;
 constexpr int kMlAt = 64;
 
+// The sequences of one launch: the i-th is ids[i] (a device list) or begin + i (a
+// contiguous range, ids == nullptr).
+struct SeqSel {
+  int32_t begin;
+  const int32_t* ids;
+  __device__ __forceinline__ int at(int i) const { return ids ? __ldg(ids + i) : begin + i; }
+};
+
 // Options of a tensor-core attend launch (all off by default).
 struct AttendOpts {
   const void* k_new = nullptr;       // fused append of one token per sequence
@@ -56,6 +64,7 @@ struct AttendOpts {
   const int32_t* list_ids = nullptr; // block list [n_seqs][list_stride], list_count[n_seqs]
   const int32_t* list_count = nullptr;
   int list_stride = 0;
+  float* tok_out = nullptr;          // entry masses also to [n_seqs][max_positions] (optional)
 };
 
 struct Dev {
@@ -202,29 +211,29 @@ inline cudaError_t smem_optin_once(std::atomic<unsigned long long>& done, Kernel
 
 struct Ctx;
 cudaError_t launch_init(const Dev& d, cudaStream_t st);
-cudaError_t launch_reset(const Dev& d, int seq_begin, int n_seqs, cudaStream_t st);
-cudaError_t launch_alloc_pages(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+cudaError_t launch_reset(const Dev& d, SeqSel sel, int n_seqs, cudaStream_t st);
+cudaError_t launch_alloc_pages(const Dev& d, int layer, SeqSel sel, int n_seqs, int n_new,
                                cudaStream_t st);
-cudaError_t launch_append(const Dev& d, int layer, int seq_begin, int n_seqs, int n_new,
+cudaError_t launch_append(const Dev& d, int layer, SeqSel sel, int n_seqs, int n_new,
                           const void* k, const void* v, cudaStream_t st);
-cudaError_t launch_attend_general(const Dev& d, int layer, int seq_begin, int n_seqs,
-                                  const void* q, float* out, cudaStream_t st);
+cudaError_t launch_attend_general(const Dev& d, int layer, SeqSel sel, int n_seqs,
+                                  const void* q, float* out, float* tok_out, cudaStream_t st);
 int accumulate_select_max_blocks();
-cudaError_t launch_accumulate_select(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+cudaError_t launch_accumulate_select(const Dev& d, SeqSel sel, int n_seqs, int max_blocks_per_seq,
                                      const int32_t* k_per_seq, int k_uniform, int score_kind, uint32_t flags,
                                      int32_t* keep_ids, int keep_capacity, int32_t* keep_count, cudaStream_t st);
-cudaError_t launch_accumulate(const Dev& d, int seq_begin, int n_seqs, int max_blocks_per_seq,
+cudaError_t launch_accumulate(const Dev& d, SeqSel sel, int n_seqs, int max_blocks_per_seq,
                               cudaStream_t st);
-cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,
+cudaError_t launch_select(const Dev& d, SeqSel sel, int n_seqs, const int32_t* k_per_seq,
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
                           int32_t* keep_count, cudaStream_t st);
 cudaError_t launch_read_ema(const Dev& d, int what, double* dst, cudaStream_t st);
 cudaError_t launch_read_trajectory(const Dev& d, float* dst, cudaStream_t st);
-cudaError_t launch_filter(const Dev& d, int seq_begin, int n_seqs, int score_kind, double theta, int32_t* ids,
+cudaError_t launch_filter(const Dev& d, SeqSel sel, int n_seqs, int score_kind, double theta, int32_t* ids,
                           int capacity, int32_t* count, cudaStream_t st);
 cudaError_t launch_clear(const Dev& d, cudaStream_t st);
 int prefill_obs_max();
-cudaError_t launch_prefill_score(const Dev& d, int layer, int seq_begin, int n_seqs, const void* q_obs, int n_obs,
+cudaError_t launch_prefill_score(const Dev& d, int layer, SeqSel sel, int n_seqs, const void* q_obs, int n_obs,
                                  int chunk_blocks, int n_chunks, cudaStream_t st);
 size_t general_smem_bytes(int Hq, int D);
 }  // namespace kvs

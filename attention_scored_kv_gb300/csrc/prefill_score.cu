@@ -71,7 +71,8 @@ struct PT {
 
 struct PSArgs {
   Dev d;
-  int layer, seq_begin, n_obs, chunk_blocks, n_chunks;
+  int layer, n_obs, chunk_blocks, n_chunks;
+  SeqSel sel;                 // the call's sequences (row sl is sequence sel.at(sl))
   const __nv_bfloat16* q;     // [n_seqs][n_obs][Hq][D]
 };
 
@@ -226,7 +227,7 @@ __global__ void __launch_bounds__(PT<PASS>::THREADS, PT<PASS>::MINB) ps_tc_kerne
   TcSmem& sm = *reinterpret_cast<TcSmem*>(base + kQBytes + P::KBYTES);
   float* votes = reinterpret_cast<float*>(base + kQBytes + P::KBYTES + sizeof(TcSmem));   // [8][nkeys]
   const Dev& d = A.d;
-  const int chunk = blockIdx.x, kvh = blockIdx.y, sl = blockIdx.z, s = A.seq_begin + sl;
+  const int chunk = blockIdx.x, kvh = blockIdx.y, sl = blockIdx.z, s = A.sel.at(sl);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SeqBlocks sb = seq_blocks(d, A.layer, s);
   const Chunk ck = chunk_of(sb, chunk, A.chunk_blocks, PASS == 2);
@@ -553,7 +554,7 @@ __global__ void ps_combine_kernel(PSArgs A, int n_seqs) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_seqs * d.Hq * kObs) return;
   const int sl = idx / (d.Hq * kObs), hr = idx % (d.Hq * kObs);
-  const SeqBlocks sb = seq_blocks(d, A.layer, A.seq_begin + sl);
+  const SeqBlocks sb = seq_blocks(d, A.layer, A.sel.at(sl));
   const int used = min((sb.n + A.chunk_blocks - 1) / A.chunk_blocks, A.n_chunks);
   float M = -INFINITY, L = 0.f;
   for (int c = 0; c < used; ++c) {
@@ -592,12 +593,12 @@ cudaError_t launch_ps(const PSArgs& A, int n_seqs, cudaStream_t st) {
 
 int prefill_obs_max() { return kObs; }
 
-cudaError_t launch_prefill_score(const Dev& d, int layer, int seq_begin, int n_seqs, const void* q_obs, int n_obs,
+cudaError_t launch_prefill_score(const Dev& d, int layer, SeqSel sel, int n_seqs, const void* q_obs, int n_obs,
                                  int chunk_blocks, int n_chunks, cudaStream_t st) {
   PSArgs A;
   A.d = d;
   A.layer = layer;
-  A.seq_begin = seq_begin;
+  A.sel = sel;
   A.n_obs = n_obs;
   A.chunk_blocks = chunk_blocks;
   A.n_chunks = n_chunks;

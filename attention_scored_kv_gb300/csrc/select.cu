@@ -51,7 +51,7 @@ __device__ __forceinline__ int block_scan(int flag, SelShared& sh, int* total) {
   return before + in_warp;
 }
 
-__global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, const int32_t* k_per_seq,
+__global__ void __launch_bounds__(kThreads) select_kernel(Dev d, SeqSel sel, const int32_t* k_per_seq,
                                                             int k_uniform, int kind, uint32_t flags, int32_t* keep_ids,
                                                             int keep_capacity, int32_t* keep_count) {
   __shared__ SelShared sh;
@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
   uint64_t* skey = reinterpret_cast<uint64_t*>(dyn);                 // [kSmemCap]
   int32_t* sid = reinterpret_cast<int32_t*>(skey + kSmemCap);        // [kSmemCap]
   int32_t* spage = sid + kSmemCap;                                   // [kSmemCap]
-  const int sl = blockIdx.x, s = seq_begin + sl;
+  const int sl = blockIdx.x, s = sel.at(sl);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int n = sb.n;
@@ -179,10 +179,10 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, int seq_begin, 
 // Threshold view ("Context views at marginal cost", Tier 1: a view filters the kept
 // table by a_s > theta): one CTA per sequence writes the resident blocks whose score
 // exceeds theta, in ascending id, 512 candidates per pass.
-__global__ void __launch_bounds__(kThreads) filter_kernel(Dev d, int seq_begin, int kind, double theta,
+__global__ void __launch_bounds__(kThreads) filter_kernel(Dev d, SeqSel sel, int kind, double theta,
                                                             int32_t* ids, int capacity, int32_t* count) {
   __shared__ SelShared sh;
-  const int sl = blockIdx.x, s = seq_begin + sl, tid = threadIdx.x;
+  const int sl = blockIdx.x, s = sel.at(sl), tid = threadIdx.x;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t steps_now = d.steps[s];
   int before = 0;
@@ -208,20 +208,20 @@ __global__ void __launch_bounds__(kThreads) filter_kernel(Dev d, int seq_begin, 
 
 }  // namespace
 
-cudaError_t launch_filter(const Dev& d, int seq_begin, int n_seqs, int score_kind, double theta, int32_t* ids,
+cudaError_t launch_filter(const Dev& d, SeqSel sel, int n_seqs, int score_kind, double theta, int32_t* ids,
                           int capacity, int32_t* count, cudaStream_t st) {
-  filter_kernel<<<n_seqs, kThreads, 0, st>>>(d, seq_begin, score_kind, theta, ids, capacity, count);
+  filter_kernel<<<n_seqs, kThreads, 0, st>>>(d, sel, score_kind, theta, ids, capacity, count);
   return cudaGetLastError();
 }
 
-cudaError_t launch_select(const Dev& d, int seq_begin, int n_seqs, const int32_t* k_per_seq,
+cudaError_t launch_select(const Dev& d, SeqSel sel, int n_seqs, const int32_t* k_per_seq,
                           int k_uniform, int score_kind, uint32_t flags, int32_t* keep_ids, int keep_capacity,
                           int32_t* keep_count, cudaStream_t st) {
   const size_t smem = (size_t)kSmemCap * (8 + 4 + 4);
   static std::atomic<unsigned long long> optin{0};   // per device
   const cudaError_t e = smem_optin_once(optin, select_kernel, (int)smem);
   if (e != cudaSuccess) return e;
-  select_kernel<<<n_seqs, kThreads, smem, st>>>(d, seq_begin, k_per_seq, k_uniform, score_kind, flags, keep_ids,
+  select_kernel<<<n_seqs, kThreads, smem, st>>>(d, sel, k_per_seq, k_uniform, score_kind, flags, keep_ids,
                                                 keep_capacity, keep_count);
   return cudaGetLastError();
 }

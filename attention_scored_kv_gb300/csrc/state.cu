@@ -23,8 +23,8 @@ __global__ void init_free_stack(Dev d) {
 }
 
 // One CTA per sequence: empty it in every layer.
-__global__ void reset_kernel(Dev d, int seq_begin) {
-  const int s = seq_begin + blockIdx.x;
+__global__ void reset_kernel(Dev d, SeqSel sel) {
+  const int s = sel.at(blockIdx.x);
   const size_t pos_base = (size_t)s * d.max_positions;
   const size_t blk_base = (size_t)s * d.max_blocks;
   for (int64_t p = threadIdx.x; p < d.max_positions; p += blockDim.x) {
@@ -127,8 +127,8 @@ cudaError_t launch_init(const Dev& d, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_reset(const Dev& d, int seq_begin, int n_seqs, cudaStream_t st) {
-  reset_kernel<<<n_seqs, 256, 0, st>>>(d, seq_begin);
+cudaError_t launch_reset(const Dev& d, SeqSel sel, int n_seqs, cudaStream_t st) {
+  reset_kernel<<<n_seqs, 256, 0, st>>>(d, sel);
   return cudaGetLastError();
 }
 

@@ -40,9 +40,11 @@
  *     stream).  No call synchronises except kvs_get_status().
  *   - Device-side failures (capacity exhausted, a bounded wait that ran out) set an
  *     error word that kvs_get_status() reports and kvs_clear_error() resets.
- *   - Sequences are addressed as a contiguous range [seq_begin, seq_begin + n_seqs)
- *     of the max_seqs sequences the cache holds; per-sequence inputs and outputs are
- *     packed in that order.
+ *   - The sequences of a call are a kvs_seqs: either a contiguous range of the
+ *     max_seqs sequences the cache holds, or a list of distinct sequence ids in any
+ *     order (a serving batch whose active sequences are scattered).  Per-sequence
+ *     inputs and outputs are packed in the call's order: row i belongs to the i-th
+ *     sequence of the range or list.
  *   - Call order per step: kvs_append_kv(l) before kvs_decode_attend(l) for every
  *     layer, kvs_accumulate_scores() after the last layer, then kvs_select_blocks().
  */
@@ -56,7 +58,7 @@
 extern "C" {
 #endif
 
-#define KVS_ABI_VERSION 1
+#define KVS_ABI_VERSION 2
 
 #if defined(__GNUC__)
 #define KVS_API __attribute__((visibility("default")))
@@ -66,6 +68,42 @@ extern "C" {
 
 typedef struct kvs_ctx kvs_ctx;
 typedef struct CUstream_st* kvs_stream_t;   /* a cudaStream_t */
+
+/* The sequences one call works on.
+ *   Range form (h_ids == NULL, d_ids == NULL): sequences begin .. begin + count - 1.
+ *   List form (both non-NULL, begin ignored): the `count` sequence ids h_ids[0..count)
+ *     in host memory and the same ids, in the same order, in device memory at d_ids.
+ *     The library reads h_ids during the call (argument checks, its per-sequence
+ *     host bookkeeping and launch plans, so no call has to read device memory); the
+ *     kernels it launches read d_ids, which must stay valid until they have run.  The
+ *     ids must be distinct and in [0, max_seqs); a list with a bad or repeated id is
+ *     rejected (KVS_ERR_INVALID_ARGUMENT) and launches nothing.  The two copies must
+ *     hold the same ids: the library cannot check d_ids without a device read.
+ * count >= 1 in both forms. */
+typedef struct {
+  int32_t begin;
+  int32_t count;
+  const int32_t* h_ids;
+  const int32_t* d_ids;
+} kvs_seqs;
+
+static inline kvs_seqs kvs_seq_range(int32_t begin, int32_t count) {
+  kvs_seqs r;
+  r.begin = begin;
+  r.count = count;
+  r.h_ids = 0;
+  r.d_ids = 0;
+  return r;
+}
+
+static inline kvs_seqs kvs_seq_list(int32_t count, const int32_t* h_ids, const int32_t* d_ids) {
+  kvs_seqs r;
+  r.begin = 0;
+  r.count = count;
+  r.h_ids = h_ids;
+  r.d_ids = d_ids;
+  return r;
+}
 
 typedef enum {
   KVS_OK = 0,
@@ -152,12 +190,15 @@ KVS_API kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t w
 /* Free the host object.  The workspace stays the caller's. */
 KVS_API kvs_status kvs_destroy(kvs_ctx* ctx);
 
-/* Empty sequences [seq_begin, seq_begin + n_seqs): next_position = 0 in every
- * layer, score tables zeroed, H2O pages returned to the pool. */
-KVS_API kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kvs_stream_t stream);
+/* Empty the sequences of `seqs`: next_position = 0 in every layer, score tables
+ * zeroed, H2O pages returned to the pool ("LLM mechanics III" §5: the processed count
+ * and the positions restart only when a sequence starts over). */
+KVS_API kvs_status kvs_reset(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream);
 
-/* Append n_new tokens to every sequence of the range in layer `layer`.
- * d_k, d_v: [n_seqs][n_new][num_kv_heads][head_dim] in in_dtype, device memory.
+/* Append n_new tokens to every sequence of `seqs` in layer `layer` (Flash-MoE "Context
+ * Optimization", FP8 KV Cache > How It Works, Encoding; Sliding Window Attention >
+ * Design; "LLM mechanics III" §1 and §5: absolute positions kept apart from slots).
+ * d_k, d_v: [seqs.count][n_new][num_kv_heads][head_dim] in in_dtype, device memory.
  * Token i of sequence s goes to absolute position next_position[layer][s] + i.
  * E4M3 storage quantises each position (all KV heads of one of K or V) with
  * scale = fl32(absmax / 240) and round-to-nearest-even saturating E4M3 codes of
@@ -165,26 +206,35 @@ KVS_API kvs_status kvs_reset(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, kv
  * Window mode writes position p to slot p % window; H2O mode writes it to the page
  * of block p / 16.  Errors: KVS_ERR_CAPACITY if a sequence would pass
  * max_positions (or, on the device, if the H2O page pool is empty). */
-KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                         int32_t n_new, const void* d_k, const void* d_v, kvs_stream_t stream);
+KVS_API kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, int32_t n_new, const void* d_k,
+                                 const void* d_v, kvs_stream_t stream);
 
-/* Decode attention of one query per head over the resident entries of layer `layer`.
- * d_q: [n_seqs][num_q_heads][head_dim] in in_dtype; d_out: [n_seqs][num_q_heads]
- * [head_dim] float32, both device memory aligned to 16 bytes.  Logits are
- * q.k/sqrt(D) (k, v decoded inline from E4M3 as code * scale), softmax per head
- * over the resident entries.
+/* Decode attention of one query per head over the resident entries of layer `layer`
+ * ("Context views at marginal cost", §7 Fact 3: the QK^T, softmax, V read; Flash-MoE
+ * "Context Optimization", FP8 KV Cache > How It Works, Decoding: E4M3 decoded inline;
+ * H2O KV Cache Eviction > How It Works in Flash-MoE, step 1: the post-softmax weights
+ * summed across all query heads; "Per-Head Attention as a Scoring Signal", Fix: score
+ * per head, place per block).
+ * d_q: [seqs.count][num_q_heads][head_dim] in in_dtype; d_out: [seqs.count]
+ * [num_q_heads][head_dim] float32, both device memory aligned to 16 bytes.  Logits
+ * are q.k/sqrt(D) (k, v decoded inline from E4M3 as code * scale), softmax per head
+ * over the resident entries; query head h reads KV head h / (Hq / Hkv).
  * In the same launch, without writing the weights anywhere off chip, the kernel
  * stores the step masses of this layer: per resident entry the sum over query heads
  * of its weight, and per resident 16-token block the maximum over query heads of
  * the head's summed weight in the block (both readable with kvs_read_state).
- * Errors: KVS_ERR_EMPTY_CACHE if a sequence of the range has no resident entry;
- * KVS_ERR_INVALID_ARGUMENT if d_q or d_out is NULL or not 16-byte aligned. */
-KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                             const void* d_q, float* d_out, kvs_stream_t stream);
+ * d_tok_mass_opt: NULL, or device float32 [seqs.count][max_positions] that also
+ * receives each resident entry's mass at its absolute position (row i for the i-th
+ * sequence of the call; elements of positions not resident are left as they were).
+ * Errors: KVS_ERR_EMPTY_CACHE if a sequence of the call has no resident entry;
+ * KVS_ERR_INVALID_ARGUMENT if d_q or d_out is NULL or not 16-byte aligned, or
+ * d_tok_mass_opt is not 4-byte aligned. */
+KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q, float* d_out,
+                                     float* d_tok_mass_opt, kvs_stream_t stream);
 
 /* One decode step of one layer in one call: kvs_append_kv of one new token per
- * sequence (d_k, d_v: [n_seqs][1][num_kv_heads][head_dim] in in_dtype), then
- * kvs_decode_attend (d_q, d_out as there).  No page counterpart as a single step: the
+ * sequence (d_k, d_v: [seqs.count][1][num_kv_heads][head_dim] in in_dtype), then
+ * kvs_decode_attend (d_q, d_out, d_tok_mass_opt as there).  No page counterpart as a single step: the
  * pages append the decode token and attend over the cache including it, and this call
  * does both.  With the tensor-core attend in NONE or WINDOW mode, and when every
  * sequence of the range can have CTAs of its own, it is one kernel launch.  The CTA
@@ -194,15 +244,15 @@ KVS_API kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  * and errors as the two calls.  If the launch reports KVS_ERR_TIMEOUT, the token may
  * be stored without next_position having advanced: append it again after
  * kvs_clear_error. */
-KVS_API kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                             const void* d_k, const void* d_v, const void* d_q, float* d_out,
-                             kvs_stream_t stream);
+KVS_API kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_k,
+                                     const void* d_v, const void* d_q, float* d_out, float* d_tok_mass_opt,
+                                     kvs_stream_t stream);
 
 /* Tier-2 re-attend ("Context views at marginal cost", Tier 2 and Fact 3): decode
  * attention of one query per head over the cached K and V of a selected subset only.
  * The subset is the resident entries of the listed blocks, for example the keep_ids
- * that kvs_select_blocks returns.  d_block_ids: [n_seqs][ids_stride] int32 block ids
- * (each listed once); d_block_count: [n_seqs] int32, the first count entries of a row
+ * that kvs_select_blocks returns.  d_block_ids: [seqs.count][ids_stride] int32 block
+ * ids (each listed once); d_block_count: [seqs.count] int32, the first count entries of a row
  * are used (clamped to [0, ids_stride]); both device memory.  d_q, d_out as in
  * kvs_decode_attend.  Softmax over the subset; no mass or score is written.  Listed
  * blocks must be resident: with every listed entry outside the resident range the
@@ -212,9 +262,9 @@ KVS_API kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  * Errors: KVS_ERR_UNSUPPORTED unless the context uses the tensor-core attend;
  * KVS_ERR_EMPTY_CACHE as kvs_decode_attend; KVS_ERR_INVALID_ARGUMENT for missing
  * buffers, ids_stride < 1 or unaligned q / out. */
-KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                             const int32_t* d_block_ids, int32_t ids_stride, const int32_t* d_block_count,
-                             const void* d_q, float* d_out, kvs_stream_t stream);
+KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const int32_t* d_block_ids,
+                                     int32_t ids_stride, const int32_t* d_block_count, const void* d_q,
+                                     float* d_out, kvs_stream_t stream);
 
 /* kvs_decode_attend without any exchange area from the caller.  No page counterpart:
  * this is a deployment variant, not a step of the method.
@@ -235,8 +285,9 @@ KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  *   KVS_ERR_UNSUPPORTED  the context does not use the tensor-core attend, or this
  *                        launch's logits do not fit in shared memory;
  *   KVS_ERR_CAPACITY     the launch needs more than the array holds:
- *                        (grid + n_seqs) * num_q_heads * head_dim * 4 bytes,
- *                        rounded up to 256, plus (grid + n_seqs) * num_q_heads * 8
+ *                        (grid + seqs.count) * num_q_heads * head_dim * 4
+ *                        bytes, rounded up to 256, plus (grid + seqs.count) *
+ *                        num_q_heads * 8
  *                        rounded up to 256, plus 384 * max_seqs bytes must be
  *                        <= 8 MiB.
  * The array is shared by every call of every context on the device and keeps the last
@@ -245,16 +296,15 @@ KVS_API kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, int32_t seq_be
  * order them.  The first call on a device looks up the array's device address (a
  * host-side API call, done once per device); make that first call before any stream
  * capture. */
-KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, int32_t seq_begin,
-                                                    int32_t n_seqs, const void* d_q, float* d_out,
-                                                    kvs_stream_t stream);
+KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q,
+                                                    float* d_out, float* d_tok_mass_opt, kvs_stream_t stream);
 
 /* SnapKV prefill scoring ("Context views at marginal cost", the per-system
  * reductions: observation window of the prompt's last queries, votes pooled per token
  * and head, max-pool kernel 7).  Call it for a layer once its prompt is appended, in
  * place of the attend of a decode step; kvs_accumulate_scores after the last layer
  * then folds the result into the tables as their first step.
- * d_q_obs: [n_seqs][n_obs][num_q_heads][head_dim] bf16 (device, 16-byte aligned), the
+ * d_q_obs: [seqs.count][n_obs][num_q_heads][head_dim] bf16 (device, 16-byte aligned), the
  * queries of the last n_obs positions of each sequence's prompt, oldest first.  Query
  * i, at position next_position - n_obs + i, attends over the resident entries at
  * positions <= its own: logits q.k/sqrt(D), softmax per head.  An entry's vote for
@@ -262,43 +312,50 @@ KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer,
  * at each resident position, the largest vote among the resident positions within 3
  * of it.  The pooled votes replace the layer's step masses: the entry mass is their
  * sum over heads, and the block mass the max over heads of the in-block sum.  E4M3
- * caches round the queries to f16, as the decode attend does.
+ * caches convert the bf16 queries to f16 (exact in f16's normal range), as the
+ * decode attend does.
  * Needs a context created with obs_window >= n_obs (tensor-core configurations
  * only).  Errors: KVS_ERR_INVALID_ARGUMENT for n_obs outside [1, obs_window], a
  * sequence holding fewer than n_obs entries, or (window mode) n_obs > window. */
-KVS_API kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, int32_t seq_begin, int32_t n_seqs,
-                                     const void* d_q_obs, int32_t n_obs, kvs_stream_t stream);
+KVS_API kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q_obs,
+                                     int32_t n_obs, kvs_stream_t stream);
 
-/* Fold this step's masses of every layer into the score tables of the range:
+/* Fold this step's masses of every layer into the score tables of the sequences of
+ * `seqs` ("Context views at marginal cost", Tier 1: EMA and Cumulative as running
+ * reductions, O(1) per span per step; Flash-MoE "Context Optimization", H2O KV Cache
+ * Eviction > How It Works in Flash-MoE, step 1: the scores accumulate over all steps;
+ * "Per-Head Attention as a Scoring Signal", Combined placement decision: a block
+ * scores as its best head):
  * token score x_p = sum over layers of the entry masses, block score y_k = max over
  * layers of the block masses; for every tracked entry (every position below
  * next_position and every block holding one) C += x and E <- d*E + (1-d)*x, x = 0
  * where nothing was attended this step.  Errors: KVS_ERR_STATE if the layers of a
  * sequence disagree on next_position. */
-KVS_API kvs_status kvs_accumulate_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
-                                 kvs_stream_t stream);
+KVS_API kvs_status kvs_accumulate_scores(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream);
 
 #define KVS_SELECT_PROTECT 1u  /* H2O: keep the sink and recent blocks first */
 #define KVS_SELECT_APPLY   2u  /* H2O: evict the unkept blocks (pages back to the pool) */
 
-/* Per sequence of the range, keep the k resident blocks with the highest score
+/* Top-budget block selection ("Per-Head Attention as a Scoring Signal", worked 128K
+ * example: the highest-scoring blocks stay resident; Flash-MoE "Context Optimization",
+ * H2O KV Cache Eviction > The Algorithm: sink, recent and heavy-hitter regions).
+ * Per sequence of `seqs`, keep the k resident blocks with the highest score
  * (C or E, a kvs_score_kind), ties to the lower block id; all are kept when k >= the
  * resident count.  With KVS_SELECT_PROTECT the blocks holding a sink token (position
  * < h2o_sink_tokens) or a recent token (position >= next_position - ceil(recent_frac
  * * budget)) are kept whatever their score and the rest of k is filled by score; if
- * they alone exceed k, all of them are kept.  k comes from d_k_per_seq ([n_seqs]
+ * they alone exceed k, all of them are kept.  k comes from d_k_per_seq ([seqs.count]
  * int32, device) or, when d_k_per_seq is NULL, from k_uniform for every sequence.
- * d_keep_ids: [n_seqs][keep_capacity] int32 (device), ascending block ids;
- * d_keep_count: [n_seqs] int32 (device), the number kept (ids beyond keep_capacity
+ * d_keep_ids: [seqs.count][keep_capacity] int32 (device), ascending block ids;
+ * d_keep_count: [seqs.count] int32 (device), the number kept (ids beyond keep_capacity
  * are dropped and flag KVS_ERR_CAPACITY on the device).
  * Errors: KVS_ERR_INVALID_ARGUMENT for APPLY outside H2O mode or a negative k. */
-KVS_API kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
-                             const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
+KVS_API kvs_status kvs_select_blocks(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
                              uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                              int32_t* d_keep_count, kvs_stream_t stream);
 
 /* kvs_accumulate_scores followed by kvs_select_blocks (same arguments as the latter),
- * in one launch when every sequence of the range has at most 512 resident blocks.
+ * in one launch when every sequence of the call has at most 512 resident blocks.
  * There is no page counterpart as a single step: the pages fold a step's weights into
  * the scores and then pick the blocks to keep, and this call does both.  The tables
  * are updated exactly as the accumulate kernel does, on its grid.  The last CTA of
@@ -306,39 +363,38 @@ KVS_API kvs_status kvs_select_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_
  * with a lower id, which keeps the same set as the radix select.  It then compacts the
  * kept ids in id order.  Longer sequences: the two calls.  Same results, state and
  * errors as the two calls. */
-KVS_API kvs_status kvs_accumulate_select(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs,
-                                 const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
+KVS_API kvs_status kvs_accumulate_select(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform, int32_t score_kind,
                                  uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                                  int32_t* d_keep_count, kvs_stream_t stream);
 
 /* Threshold view ("Context views at marginal cost", Tier 1: a view is a filter of the
- * kept score table, a_s > theta): per sequence of the range, the resident blocks whose
+ * kept score table, a_s > theta): per sequence of `seqs`, the resident blocks whose
  * block score (a kvs_score_kind, read as kvs_select_blocks reads it) is strictly
- * greater than theta, in ascending id.  d_ids: [n_seqs][capacity] int32 (device);
- * d_count: [n_seqs] int32 (device), the number that passed (ids beyond capacity are
+ * greater than theta, in ascending id.  d_ids: [seqs.count][capacity] int32 (device);
+ * d_count: [seqs.count] int32 (device), the number that passed (ids beyond capacity are
  * dropped and flag KVS_ERR_CAPACITY on the device).  Reads the tables only.
  * Errors: KVS_ERR_INVALID_ARGUMENT for an unknown score kind, a NaN theta or missing
  * buffers. */
-KVS_API kvs_status kvs_filter_blocks(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, int32_t score_kind,
-                                     double theta, int32_t* d_ids, int32_t capacity, int32_t* d_count,
+KVS_API kvs_status kvs_filter_blocks(kvs_ctx* ctx, kvs_seqs seqs, int32_t score_kind, double theta, int32_t* d_ids, int32_t capacity, int32_t* d_count,
                                      kvs_stream_t stream);
 
 /* Score snapshot (the side-car kept next to the session's KV: "Context views at
- * marginal cost", Tier 1).  Export copies, for the sequences of the range, every score
- * table (token and block cumulative, EMA and update stamps, token-sum and TOVA block
- * scores, the trajectory ring, the layer profiles) and the step counts into one
- * buffer; import copies such a buffer back into a range of the same length.  The
+ * marginal cost", Tier 1).  Export copies, for the sequences of `seqs` in the call's
+ * order, every score table (token and block cumulative, EMA and update stamps,
+ * token-sum and TOVA block scores, the trajectory ring, the layer profiles) and the
+ * step counts into one buffer; import copies such a buffer back into as many
+ * sequences (any range or list of the same count).  The
  * buffer is raw and carries no header: it can be imported only into a context created
  * with the same max_positions, traj_len and profile_layers (the KV entries and the
  * residency are not part of it).  The buffer may be device memory or host memory
  * (pinned memory keeps the copies asynchronous); it must hold
- * kvs_scores_snapshot_bytes(ctx, n_seqs) bytes.  One cudaMemcpyAsync per table on
- * `stream`.  Errors: KVS_ERR_CAPACITY for a short buffer. */
+ * kvs_scores_snapshot_bytes(ctx, seqs.count) bytes.  One cudaMemcpyAsync per table on
+ * `stream` (range form) or per table and sequence (list form).  Errors: KVS_ERR_CAPACITY for a short buffer. */
 KVS_API size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs);
-KVS_API kvs_status kvs_export_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, void* dst, size_t dst_bytes,
+KVS_API kvs_status kvs_export_scores(kvs_ctx* ctx, kvs_seqs seqs, void* dst, size_t dst_bytes,
                                      kvs_stream_t stream);
-KVS_API kvs_status kvs_import_scores(kvs_ctx* ctx, int32_t seq_begin, int32_t n_seqs, const void* src,
-                                     size_t src_bytes, kvs_stream_t stream);
+KVS_API kvs_status kvs_import_scores(kvs_ctx* ctx, kvs_seqs seqs, const void* src, size_t src_bytes,
+                                     kvs_stream_t stream);
 
 /* State read-back (tests, inspection).  Copies one array of `layer` (ignored for
  * per-sequence items) into d_dst (device), which must hold kvs_state_bytes(). */

@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported():
 
 
 def test_abi_version_and_status_strings():
-    assert kvs.lib().kvs_abi_version() == 1
+    assert kvs.lib().kvs_abi_version() == 2
     for s in range(8):
         assert kvs.status_string(s)
     assert kvs.status_string(3).startswith("empty cache")
