@@ -69,9 +69,10 @@ def block_step_mass(weights, positions, block_tokens=16):
     weights = np.asarray(weights, dtype=np.float64)
     positions = np.asarray(positions, dtype=np.int64)
     blocks = positions // block_tokens
-    out = {}
-    for k in np.unique(blocks):
-        sel = blocks == k
-        per_head = np.sum(weights[:, sel], axis=1)
-        out[int(k)] = float(np.max(per_head))
-    return out
+    # group the entries by block (a stable sort keeps each block's entries in order),
+    # sum each head's weights over every group, then take the max over heads
+    order = np.argsort(blocks, kind="stable")
+    ids, starts = np.unique(blocks[order], return_index=True)
+    per_head = np.add.reduceat(weights[:, order], starts, axis=1)     # [Hq, blocks]
+    best = np.max(per_head, axis=0)
+    return {int(k): float(m) for k, m in zip(ids, best)}

@@ -91,3 +91,23 @@ def test_token_mass_sums_to_heads():
     k = rng.normal(size=(40, 2, 32))
     _, w = attention.decode_attention(q, k, k)
     assert abs(attention.token_step_mass(w).sum() - 8.0) < 1e-12
+
+
+def test_block_mass_brute_force_any_order():
+    """Block masses equal a per-block loop written out by hand, for positions in any
+    order and blocks with gaps (an H2O residency)."""
+    rng = np.random.default_rng(8)
+    pos = np.concatenate([np.arange(0, 20), np.arange(64, 90), np.arange(200, 205)])
+    perm = rng.permutation(len(pos))
+    w = rng.dirichlet(np.ones(len(pos)), size=5)
+    bm = attention.block_step_mass(w[:, perm], pos[perm], 16)
+    assert set(bm) == {0, 1, 4, 5, 12}
+    for k in bm:
+        best = 0.0
+        for h in range(5):
+            s = 0.0
+            for j in range(len(pos)):
+                if pos[j] // 16 == k:
+                    s += w[h, j]
+            best = max(best, s)
+        assert abs(bm[k] - best) <= 1e-15
