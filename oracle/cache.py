@@ -47,7 +47,8 @@ class ScoreTables:
       marginal cost", the per-system reductions).
     """
 
-    def __init__(self, max_positions, block_tokens=16, ema_decay=0.9, traj_len=0, profile_layers=()):
+    def __init__(self, max_positions, block_tokens=16, ema_decay=0.9, traj_len=0, profile_layers=(),
+                 profile_heads=()):
         self.block_tokens = block_tokens
         self.d = float(ema_decay)
         nb = -(-max_positions // block_tokens)
@@ -58,6 +59,10 @@ class ScoreTables:
         self.traj = np.zeros((traj_len, nb))
         self.profile_layers = tuple(profile_layers)
         self.prof = np.zeros((len(self.profile_layers), nb))
+        # per-head profiles ("within head H" of a retrieval-head subset): per profiled
+        # (layer, query head), the sum over steps of that head's in-block weight
+        self.profile_heads = tuple(profile_heads)
+        self.hprof = np.zeros((len(self.profile_heads), nb))
         self.c_tok = np.zeros(max_positions)
         self.e_tok = np.zeros(max_positions)
         self.c_blk = np.zeros(nb)
@@ -76,7 +81,7 @@ class ScoreTables:
                 out[:, j] = self.traj[step % self.traj_len]
         return out
 
-    def update(self, tracked_positions, x_tok, y_blk, layer_blk=None):
+    def update(self, tracked_positions, x_tok, y_blk, layer_blk=None, head_blk=None):
         """One step.  x_tok: float64 array over positions 0..tracked_positions-1 with
         the step's token scores (0 where nothing attended); y_blk: float64 array over
         the blocks holding a tracked position, likewise.  Every tracked entry is
@@ -103,6 +108,9 @@ class ScoreTables:
         for i, l in enumerate(self.profile_layers):
             for k, m in layer_blk[l].items():
                 self.prof[i, k] += m
+        for i in range(len(self.profile_heads)):
+            for k, m in head_blk[i].items():
+                self.hprof[i, k] += m
         self.steps += 1
 
 
@@ -112,7 +120,7 @@ class OracleKV:
     def __init__(self, *, num_layers, num_q_heads, num_kv_heads, head_dim, num_seqs,
                  max_positions, kv_format="bf16", window=0, h2o_budget_tokens=0,
                  h2o_sink_tokens=4, h2o_recent_frac=0.25, ema_decay=0.9, block_tokens=16, traj_len=0,
-                 profile_layers=()):
+                 profile_layers=(), profile_heads=()):
         if num_q_heads % num_kv_heads:
             raise ValueError("num_q_heads must be a multiple of num_kv_heads")
         if window < 0:
@@ -150,8 +158,11 @@ class OracleKV:
             self.k_vals = np.zeros(shape, dtype=np.float32)
             self.v_vals = np.zeros(shape, dtype=np.float32)
         self.resident_blocks = [set() for _ in range(num_seqs)]      # H2O mode only
-        self.scores = [ScoreTables(max_positions, block_tokens, ema_decay, traj_len, profile_layers)
+        self.profile_heads = tuple((int(l), int(h)) for l, h in profile_heads)
+        self.scores = [ScoreTables(max_positions, block_tokens, ema_decay, traj_len, profile_layers,
+                                   self.profile_heads)
                        for _ in range(num_seqs)]
+        self._head_blk = {}      # (l, b, h) -> {block: in-block weight of head h} of the latest attend
         self._tok_mass = {}      # (l, b) -> (positions, token mass) of the latest attend
         self._blk_mass = {}      # (l, b) -> {block: mass} of the latest attend
         self._attended = set()   # (l, b) attended since the last accumulate
@@ -218,8 +229,15 @@ class OracleKV:
         out, w = attention.decode_attention(q, k, v)
         self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(w))
         self._blk_mass[(layer, seq)] = attention.block_step_mass(w, pos, self.block)
+        self._record_heads(layer, seq, w, pos)
         self._attended.add((layer, seq))
         return out, w, pos
+
+    def _record_heads(self, layer, seq, w, pos):
+        # one head's in-block weight sum: the block mass of that head alone
+        for l, h in self.profile_heads:
+            if l == layer:
+                self._head_blk[(l, seq, h)] = attention.block_step_mass(w[h:h + 1], pos, self.block)
 
     def attend_blocks(self, layer, seq, q, block_ids):
         """Tier-2 re-attend ("Context views at marginal cost", Tier 2 and Fact 3): a new
@@ -251,6 +269,7 @@ class OracleKV:
         pooled = snapkv.max_pool(votes, pos, kernel)
         self._tok_mass[(layer, seq)] = (pos, attention.token_step_mass(pooled))
         self._blk_mass[(layer, seq)] = attention.block_step_mass(pooled, pos, self.block)
+        self._record_heads(layer, seq, pooled, pos)
         self._attended.add((layer, seq))
         return votes, pooled, pos
 
@@ -285,7 +304,8 @@ class OracleKV:
                 for k, m in self._blk_mass[(l, b)].items():
                     y_blk[k] = max(y_blk[k], m)        # max over layers
                 layer_blk[l] = self._blk_mass[(l, b)]
-            self.scores[b].update(n, x_tok, y_blk, layer_blk)
+            head_blk = [self._head_blk[(l, b, h)] for l, h in self.profile_heads]
+            self.scores[b].update(n, x_tok, y_blk, layer_blk, head_blk)
             result[b] = (x_tok, y_blk)
         return result
 

@@ -71,3 +71,39 @@ def test_layer_profiles():
                     ref[k] += m
             assert np.allclose(sc.prof[i], ref, rtol=0, atol=1e-12)
             assert np.all(sc.prof[i] <= sc.c_blk + 1e-12)
+
+
+def _head_run(L=2, hq=4, hkv=2, window=0, steps=20, prefill=37, heads=((0, 1), (1, 3)), seed=5):
+    rng = np.random.default_rng(seed)
+    D = 16
+    o = OracleKV(num_layers=L, num_q_heads=hq, num_kv_heads=hkv, head_dim=D, num_seqs=1,
+                 max_positions=prefill + steps, kv_format="f32", window=window, profile_heads=heads)
+    for l in range(L):
+        o.append(l, 0, rng.normal(size=(prefill, hkv, D)), rng.normal(size=(prefill, hkv, D)))
+    for t in range(steps):
+        for l in range(L):
+            o.append(l, 0, rng.normal(size=(1, hkv, D)), rng.normal(size=(1, hkv, D)))
+            o.attend(l, 0, rng.normal(size=(hq, D)) * 2)
+        o.accumulate()
+    return o
+
+
+@pytest.mark.parametrize("window", [0, 21])
+def test_head_profiles_hold_one_unit_of_weight_per_step(window):
+    """A head's weights sum to one over the resident entries every step, so its
+    profile summed over the blocks equals the number of steps; and a single head's
+    in-block sum never exceeds the block mass (the max over heads and layers), so the
+    profile stays under the cumulative block score."""
+    o = _head_run(window=window)
+    sc = o.scores[0]
+    for i in range(len(sc.profile_heads)):
+        assert abs(sc.hprof[i].sum() - sc.steps) <= 1e-12 * sc.steps
+        assert np.all(sc.hprof[i] <= sc.c_blk + 1e-12)
+
+
+def test_head_profile_of_the_only_head_is_the_cumulative_block_score():
+    """With one layer and one query head the block mass is that head's in-block sum,
+    so the head's profile is the cumulative block score itself."""
+    o = _head_run(L=1, hq=1, hkv=1, heads=((0, 0),))
+    sc = o.scores[0]
+    assert np.array_equal(sc.hprof[0], sc.c_blk)
