@@ -21,7 +21,7 @@ from ._abi import (  # noqa: F401
 from ._abi import (  # noqa: F401
     STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
     STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
-    STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE,
+    STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE, STATE_HEAD_PROFILE,
 )
 
 _TORCH_DT = {F32: torch.float32, BF16: torch.bfloat16}

@@ -5,6 +5,7 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_lib", "libkvs.so")
+LIB_DEBUG_PATH = os.path.join(HERE, "_lib", "libkvs_debug.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "kvs.h")
 
 # kvs_status
@@ -24,7 +25,7 @@ SELECT_PROTECT, SELECT_APPLY = 1, 2
 # kvs_state_item
 (STATE_K_PAGES, STATE_V_PAGES, STATE_K_SCALES, STATE_V_SCALES, STATE_POSITIONS, STATE_NEXT_POSITION,
  STATE_TOKEN_MASS, STATE_BLOCK_MASS, STATE_C_TOKEN, STATE_E_TOKEN, STATE_C_BLOCK, STATE_E_BLOCK, STATE_STEPS,
- STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE) = range(18)
+ STATE_BLOCK_TABLE, STATE_S_BLOCK, STATE_T_BLOCK, STATE_TRAJECTORY, STATE_LAYER_PROFILE, STATE_HEAD_PROFILE) = range(19)
 
 
 class Config(ctypes.Structure):
@@ -35,7 +36,7 @@ class Config(ctypes.Structure):
         ("h2o_sink_tokens", ctypes.c_int32), ("num_pages", ctypes.c_int32), ("kernel", ctypes.c_int32),
         ("spin_limit", ctypes.c_int32), ("kv_dtype", ctypes.c_int32), ("in_dtype", ctypes.c_int32),
         ("traj_len", ctypes.c_int32), ("profile_layers", ctypes.c_uint32), ("obs_window", ctypes.c_int32),
-        ("reserved_i", ctypes.c_int32 * 2),
+        ("n_profile_heads", ctypes.c_int32), ("profile_heads", ctypes.c_int32 * 4), ("reserved_i", ctypes.c_int32),
         ("h2o_recent_frac", ctypes.c_double), ("ema_decay", ctypes.c_double),
         ("reserved_d", ctypes.c_double * 2),
     ]
@@ -84,16 +85,20 @@ _SIGS = {
     "kvs_last_error": (ctypes.c_char_p, [_P]),
     "kvs_status_string": (ctypes.c_char_p, [_I]),
     "kvs_abi_version": (_I, []),
+    "kvs_build_info": (ctypes.c_uint32, []),
 }
 
 _lib = None
 
 
-def load(path=LIB_PATH):
-    """Load libkvs.so once.  Raises if it has not been built: there is no fallback."""
+def load(path=None):
+    """Load libkvs.so once (libkvs_debug.so when KVS_LIB_VARIANT=debug).  Raises if it
+    has not been built: there is no fallback."""
     global _lib
     if _lib is not None:
         return _lib
+    if path is None:
+        path = LIB_DEBUG_PATH if os.environ.get("KVS_LIB_VARIANT", "") == "debug" else LIB_PATH
     if not os.path.exists(path):
         raise RuntimeError("libkvs.so is not built (%s); run python -m attention_scored_kv_gb300.build" % path)
     lib = ctypes.CDLL(path)

@@ -1,7 +1,9 @@
 """Build libkvs.so in-tree with nvcc for sm_103a (GB300).
 
 Each CUDA translation unit is compiled in parallel to an object under _build/, then
-linked into attention_scored_kv_gb300/_lib/libkvs.so.  No cmake, no torch extension
+linked into attention_scored_kv_gb300/_lib/libkvs.so.  The same sources built with
+-DKVS_DEBUG (device-side bounds checks, NaN-poisoned scratch) give _lib/libkvs_debug.so,
+which the binding loads when KVS_LIB_VARIANT=debug.  No cmake, no torch extension
 machinery: plain nvcc, one -gencode.  Rebuilds only what changed (by mtime).
 """
 
@@ -17,6 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIBDIR = os.path.join(HERE, "_lib")
 LIB = os.path.join(LIBDIR, "libkvs.so")
+LIB_DEBUG = os.path.join(LIBDIR, "libkvs_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -41,8 +44,8 @@ def _deps():
     return max(os.path.getmtime(h) for h in hdrs)
 
 
-def _compile(src, extra):
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src, extra, objdir=BUILD):
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _deps()):
         return obj, ""
     cmd = [nvcc()] + ARCH + FLAGS + extra + ["-c", src, "-o", obj]
@@ -52,24 +55,36 @@ def _compile(src, extra):
     return obj, r.stderr
 
 
-def build(verbose=False, ptxas_info=False):
-    """Compile every translation unit and link libkvs.so; returns the library path."""
+def _link(objs, lib):
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", lib] + objs
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
+
+
+def build(verbose=False, ptxas_info=False, debug=True):
+    """Compile every translation unit and link libkvs.so (and, with debug, the checked
+    variant libkvs_debug.so); returns the release library's path."""
+    dbg_dir = os.path.join(BUILD, "debug")
     os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(dbg_dir, exist_ok=True)
     os.makedirs(LIBDIR, exist_ok=True)
     extra = ["-Xptxas", "-v"] if ptxas_info else []
     srcs = sources()
-    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        results = list(ex.map(lambda s: _compile(s, extra), srcs))
-    objs = [o for o, _ in results]
+    jobs = [(src, extra, BUILD) for src in srcs]
+    if debug:
+        jobs += [(src, ["-DKVS_DEBUG"], dbg_dir) for src in srcs]
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(16, len(jobs))) as ex:
+        results = list(ex.map(lambda j: _compile(*j), jobs))
     if verbose:
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [nvcc()] + ARCH + ["-shared", "-Xcompiler", "-fPIC", "-o", LIB] + objs
-        r = subprocess.run(cmd, capture_output=True, text=True)
-        if r.returncode != 0:
-            raise RuntimeError("link failed:\n%s\n%s" % (" ".join(cmd), r.stderr))
+    n = len(srcs)
+    _link([o for o, _ in results[:n]], LIB)
+    if debug:
+        _link([o for o, _ in results[n:]], LIB_DEBUG)
     return LIB
 
 

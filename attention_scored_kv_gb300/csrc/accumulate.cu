@@ -11,6 +11,7 @@ constexpr int kBlocksPerCta = 16;     // 16 blocks x 16 positions = 256 threads
 
 __global__ void __launch_bounds__(256) accumulate_kernel(Dev d, SeqSel sel) {
   const int s = sel.at(blockIdx.y);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
   const int i = blockIdx.x * kBlocksPerCta + (threadIdx.x >> 4);

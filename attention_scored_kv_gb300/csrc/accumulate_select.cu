@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kThreads) accumulate_select_kernel(Dev d, SeqS
   __shared__ int32_t s_take;
   const int lane_id = threadIdx.x & 31, warp_id = threadIdx.x >> 5;
   const int sl = blockIdx.y, s = sel.at(sl), tid = threadIdx.x;
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t step = d.steps[s];            // read by every CTA before the last ticket
 

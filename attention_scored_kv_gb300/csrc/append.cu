@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kWarps * 32) append_kernel(Dev d, int layer, S
                                                                const void* k_in, const void* v_in) {
   const int s_local = blockIdx.y;
   const int s = sel.at(s_local);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t np_idx = (size_t)layer * d.max_seqs + s;
   const int64_t next0 = d.next_pos[np_idx];
@@ -72,6 +73,7 @@ __global__ void alloc_pages_kernel(Dev d, int layer, SeqSel sel, int n_seqs, int
   const int sl = blockIdx.x * blockDim.x + threadIdx.x;
   if (sl >= n_seqs) return;
   const int s = sel.at(sl);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const int64_t next0 = d.next_pos[(size_t)layer * d.max_seqs + s];
   const int64_t last = next0 + n_new - 1;
   if (n_new <= 0 || last >= d.max_positions) return;   // the append reports capacity

@@ -70,6 +70,7 @@ __global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int lay
   float* lh = mh + d.Hq;                           // [Hq] sum
   float* red = lh + d.Hq;                          // [32]
   const int sl = blockIdx.x, s = sel.at(sl);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const SeqBlocks sb = seq_blocks(d, layer, s);
   const int n = sb.n * kBlock;                     // entries incl. masked ones
   if (n == 0 || n > cap) {
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kThreads) attend_general_kernel(Dev d, int lay
       float bs = 0.f;
       for (int j = 0; j < kBlock; ++j) bs += exp2f(lg[(size_t)h * cap + i * kBlock + j] - mh[h]) / lh[h];
       best = fmaxf(best, bs);
+      record_head(d, layer, s, k, h, bs);
     }
     d.blk_mass[(size_t)layer * d.blk_layer_elems + (size_t)s * d.max_blocks + k] = best;
   }

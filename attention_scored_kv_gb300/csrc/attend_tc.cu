@@ -547,6 +547,20 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
+#ifdef KVS_DEBUG
+  // every sequence id of a device list in range, or nobody touches anything
+  {
+    bool ids_ok = true;
+    for (int b = 0; b < P.n_seqs; ++b) {
+      const int s = P.sel.at(b);
+      ids_ok = ids_ok && s >= 0 && s < d.max_seqs;
+    }
+    if (!ids_ok) {
+      if (tid == 0) set_error(d, kErrBounds);
+      return;
+    }
+  }
+#endif
   // Fused append: the normaliser warp of the CTA that will hold the newest block (the
   // sequence's last CTA when every CTA has blocks) reads the new K and V rows now,
   // before this SM's copies queue up ahead of any load.
@@ -718,7 +732,8 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             const uint32_t fb = full0 + 8 * st;
             mbar_expect_tx(fb, nb * (C::BLK + (FP8 ? kBlock * 4 : 0)));
             for (int j = 0; j < nb; ++j) {
-              const int page = pages[g0 + j];
+              int page = pages[g0 + j];
+              if (!KVS_DCHECK(d, page >= 0 && page < d.num_pages)) page = 0;
               const uint32_t dst = smem_u32(ring + (size_t)st * C::STAGE + (size_t)j * C::BLK);
               tma_load_4d(dst, map, 0, 0, 0, page, fb, pol);
               if constexpr (FP8) {
@@ -749,20 +764,25 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
       const int s = P.sel.at(cseq);
       const int64_t pnew = sbw.next - 1;
       int32_t slot;
-      const int32_t page = page_of(d, s, pnew, &slot);
+      int32_t page = page_of(d, s, pnew, &slot);
+      const bool have_page = page >= 0 && page < d.num_pages;   // (H2O: allocated before the launch)
+      if (!have_page) {                         // the pool ran dry: reported, nothing stored
+        if (lane == 0) set_error(d, kErrCapacity);
+        page = 0;
+      }
       const size_t src_elem = (size_t)cseq * HKV * kD;
       const size_t lay_slot0 = (size_t)P.layer * d.slot_layer_elems + (size_t)page * kBlock;
       if (!preloaded) {                         // (a sequence with fewer blocks than CTAs)
         load_position_bf16(P.k_new, src_elem, lane, knew);
         load_position_bf16(P.v_new, src_elem, lane, vnew);
       }
-      for (int kv = 0; kv < 2; ++kv) {
+      for (int kv = 0; kv < 2 && have_page; ++kv) {
         uint8_t* base = (kv == 0 ? d.k_pages : d.v_pages) + P.layer * d.page_layer_bytes + (size_t)page * d.page_bytes;
         float* scales = kv == 0 ? d.k_scales : d.v_scales;
         store_position_regs<FP8 ? KVS_E4M3 : KVS_BF16>(d, kv == 0 ? knew : vnew, base,
                                                         scales ? scales + lay_slot0 + slot : nullptr, slot, lane);
       }
-      if (lane == 0) d.pos[lay_slot0 + slot] = pnew;
+      if (lane == 0 && have_page) d.pos[lay_slot0 + slot] = pnew;
       asm volatile("fence.proxy.async.global;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
@@ -1140,6 +1160,10 @@ attend_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant_
             }
             if (c4 == 0)
               d.blk_mass[(size_t)P.layer * d.blk_layer_elems + (size_t)s * d.max_blocks + blk_id[i]] = bm;
+            if (c4 == 1)                          // per-head profiles: the head's in-block weight
+              for (int jh = 0; jh < d.n_hprof; ++jh)
+                if (d.hprof_layer[jh] == P.layer)
+                  record_head(d, P.layer, s, blk_id[i], d.hprof_head[jh], bsi[d.hprof_head[jh]] * cfac[d.hprof_head[jh]]);
           }
         }
         }

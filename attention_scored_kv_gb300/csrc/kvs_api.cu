@@ -5,8 +5,10 @@
 // checked and sized without reading device memory.  The device holds the truth; a
 // replayed CUDA graph advances the device state but not these shadows.
 #include <cuda.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
+#include <cstdlib>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -37,6 +39,29 @@ namespace {
 
 constexpr int32_t kDefaultSpin = 5000000;   // ~0.5 s of 100 ns polls
 
+// NVTX ranges around every ABI call, for profiler timelines (Nsight Systems, ncu's
+// range filters): on when the environment variable KVS_NVTX is set to anything but
+// "0" when the library is first used.  Without an attached tool the calls do nothing.
+bool tracing_on() {
+  static const bool on = [] {
+    const char* v = std::getenv("KVS_NVTX");
+    return v && *v && std::strcmp(v, "0") != 0;
+  }();
+  return on;
+}
+
+struct Trace {
+  explicit Trace(const char* name) : on(tracing_on()) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~Trace() {
+    if (on) nvtxRangePop();
+  }
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+  bool on;
+};
+
 struct Plan {
   int mode = 0, pages_per_seq = 0, num_pages = 0, max_blocks = 0, res_blocks_per_seq = 0;
   int recent_tokens = 0;
@@ -44,7 +69,7 @@ struct Plan {
   // region offsets
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
-  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, traj, prof, steps, acc_tickets;
+  size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, traj, prof, hstep, hprof, steps, acc_tickets;
   size_t partials, part_ml, counters, logits, ps_part, ps_stat, ps_tok, ps_blk, ps_tickets, err;
   int ps_bound = 0, ps_chunks = 0;
 };
@@ -95,7 +120,22 @@ kvs_status check_config(const kvs_config* c, char* msg, size_t n) {
     put(msg, n, "profile_layers: at most 4 bits, each below num_layers");
     return KVS_ERR_INVALID_ARGUMENT;
   }
-  for (int i = 0; i < 2; ++i) if (c->reserved_i[i]) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->reserved_i) { put(msg, n, "reserved fields must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
+  if (c->n_profile_heads < 0 || c->n_profile_heads > 4) {
+    put(msg, n, "n_profile_heads must be in [0, 4]");
+    return KVS_ERR_INVALID_ARGUMENT;
+  }
+  for (int i = 0; i < c->n_profile_heads; ++i) {
+    const int l = c->profile_heads[i] >> 16, h = c->profile_heads[i] & 0xffff;
+    if (c->profile_heads[i] < 0 || l >= c->num_layers || h >= c->num_q_heads) {
+      put(msg, n, "profile_heads[%d]: layer * 65536 + query head, both in range", i);
+      return KVS_ERR_INVALID_ARGUMENT;
+    }
+    for (int j = 0; j < i; ++j)
+      if (c->profile_heads[j] == c->profile_heads[i]) { put(msg, n, "profile_heads[%d] repeats a head", i); return KVS_ERR_INVALID_ARGUMENT; }
+  }
+  for (int i = c->n_profile_heads; i < 4; ++i)
+    if (c->profile_heads[i]) { put(msg, n, "unused profile_heads entries must be 0"); return KVS_ERR_INVALID_ARGUMENT; }
   if (c->obs_window < 0 || c->obs_window > prefill_obs_max()) {
     put(msg, n, "obs_window must be in [0, %d]", prefill_obs_max());
     return KVS_ERR_INVALID_ARGUMENT;
@@ -171,6 +211,8 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->t_blk = take(B * MB * 8);
   p->traj = take(B * MB * (size_t)c->traj_len * 4);
   p->prof = take(B * MB * (size_t)__builtin_popcount(c->profile_layers) * 8);
+  p->hstep = take(c->n_profile_heads ? B * MB * 4 * 4 : 0);
+  p->hprof = take(B * MB * (size_t)c->n_profile_heads * 8);
   p->last_blk = take(B * MB * 4);
   p->steps = take(B * 4);
   p->acc_tickets = take(B * 4);
@@ -274,7 +316,8 @@ namespace {
 // Sections of a score snapshot of n sequences starting at seq_begin, in snapshot order,
 // each starting on a 256-byte boundary: the table's first element of seq_begin and the
 // bytes of the n sequences' rows.  Returns the number of sections.
-int snapshot_sections(const kvs_ctx* ctx, int seq_begin, int n, void* ptr[11], size_t bytes[11]) {
+constexpr int kSnapSections = 12;
+int snapshot_sections(const kvs_ctx* ctx, int seq_begin, int n, void* ptr[kSnapSections], size_t bytes[kSnapSections]) {
   const Dev& d = ctx->dev;
   const size_t P = d.max_positions, MB = d.max_blocks, s0 = seq_begin, TL = d.traj_len, NP = d.n_prof;
   int i = 0;
@@ -286,6 +329,7 @@ int snapshot_sections(const kvs_ctx* ctx, int seq_begin, int n, void* ptr[11], s
   add(d.s_blk + s0 * MB, n * MB * 8);
   add(d.t_blk + s0 * MB, n * MB * 8);
   add(d.prof + s0 * MB * NP, n * MB * NP * 8);
+  add(d.hprof + s0 * MB * d.n_hprof, n * MB * (size_t)d.n_hprof * 8);
   add(d.traj + s0 * MB * TL, n * MB * TL * 4);
   add(d.last_tok + s0 * P, n * P * 4);
   add(d.last_blk + s0 * MB, n * MB * 4);
@@ -309,11 +353,11 @@ kvs_status snapshot_copy(kvs_ctx* ctx, const kvs_seqs& seqs, void* buf, size_t b
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   uint8_t* b = static_cast<uint8_t*>(buf);
   const bool list = seqs.h_ids != nullptr;
-  void* ptr[11];
-  size_t bytes[11];
+  void* ptr[kSnapSections];
+  size_t bytes[kSnapSections];
   const int ns = snapshot_sections(ctx, list ? 0 : seqs.begin, n, ptr, bytes);
-  void* row0[11];
-  size_t rowb[11];
+  void* row0[kSnapSections];
+  size_t rowb[kSnapSections];
   snapshot_sections(ctx, 0, 1, row0, rowb);                  // one sequence's row of each table
   size_t off = 0;
   for (int i = 0; i < ns; ++i) {
@@ -402,6 +446,7 @@ void shrink_h2o_bounds(kvs_ctx* ctx, uint32_t flags, const int32_t* d_k_per_seq,
 extern "C" {
 
 void kvs_config_init(kvs_config* cfg) {
+  Trace trace_("kvs_config_init");
   if (!cfg) return;
   std::memset(cfg, 0, sizeof *cfg);
   cfg->num_layers = 1;
@@ -419,10 +464,12 @@ void kvs_config_init(kvs_config* cfg) {
 }
 
 kvs_status kvs_validate_config(const kvs_config* cfg, char* msg, size_t msg_len) {
+  Trace trace_("kvs_validate_config");
   return check_config(cfg, msg, msg_len);
 }
 
 size_t kvs_workspace_bytes(const kvs_config* cfg) {
+  Trace trace_("kvs_workspace_bytes");
   if (check_config(cfg, nullptr, 0) != KVS_OK) return 0;
   Plan p;
   make_plan(cfg, &p);
@@ -431,6 +478,7 @@ size_t kvs_workspace_bytes(const kvs_config* cfg) {
 
 kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace_bytes, kvs_stream_t stream,
                       kvs_ctx** out) {
+  Trace trace_("kvs_create");
   if (!out) return KVS_ERR_INVALID_ARGUMENT;
   *out = nullptr;
   char msg[256];
@@ -492,6 +540,13 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.n_prof = 0;
   for (int l = 0; l < cfg->num_layers && l < 32; ++l)
     if (cfg->profile_layers >> l & 1u) d.prof_layer[d.n_prof++] = l;
+  d.hstep = reinterpret_cast<float*>(w + p.hstep);
+  d.hprof = reinterpret_cast<double*>(w + p.hprof);
+  d.n_hprof = cfg->n_profile_heads;
+  for (int j = 0; j < cfg->n_profile_heads; ++j) {
+    d.hprof_layer[j] = cfg->profile_heads[j] >> 16;
+    d.hprof_head[j] = cfg->profile_heads[j] & 0xffff;
+  }
   d.last_blk = reinterpret_cast<int32_t*>(w + p.last_blk);
   d.steps = reinterpret_cast<int32_t*>(w + p.steps);
   d.acc_tickets = reinterpret_cast<int32_t*>(w + p.acc_tickets);
@@ -533,17 +588,33 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     delete ctx;
     return KVS_ERR_CUDA;
   }
+#ifdef KVS_DEBUG
+  // Debug builds fill every region that must be written before it is read with 0xFF
+  // bytes (NaN as float, NaN pairs as (m, l) words): a read of a stale or never-written
+  // element then shows up as a non-finite result.
+  {
+    const size_t regions[][2] = {{p.tok_mass, p.blk_mass}, {p.blk_mass, p.next_pos}, {p.hstep, p.hprof},
+                                 {p.partials, p.counters}, {p.logits, p.ps_part}, {p.ps_part, p.ps_tickets}};
+    for (const auto& r : regions)
+      if (r[1] > r[0] && cudaMemsetAsync(w + r[0], 0xFF, r[1] - r[0], s) != cudaSuccess) {
+        delete ctx;
+        return KVS_ERR_CUDA;
+      }
+  }
+#endif
   *out = ctx;
   return KVS_OK;
 }
 
 kvs_status kvs_destroy(kvs_ctx* ctx) {
+  Trace trace_("kvs_destroy");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   delete ctx;
   return KVS_OK;
 }
 
 kvs_status kvs_reset(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream) {
+  Trace trace_("kvs_reset");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
@@ -559,6 +630,7 @@ kvs_status kvs_reset(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream) {
 
 kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, int32_t n_new, const void* d_k,
                          const void* d_v, kvs_stream_t stream) {
+  Trace trace_("kvs_append_kv");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -596,6 +668,7 @@ kvs_status kvs_append_kv(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, int32_t n_n
 
 kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q, float* d_out,
                              float* d_tok_mass_opt, kvs_stream_t stream) {
+  Trace trace_("kvs_decode_attend");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -608,16 +681,19 @@ kvs_status kvs_decode_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
   if (ctx->kernel == KVS_KERNEL_TENSOR) {
     AttendOpts opt;
     opt.tok_out = d_tok_mass_opt;
-    return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
-                                         seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt, cs),
-                   "tensor-core attend");
-  }
-  return cuda_ok(ctx, launch_attend_general(ctx->dev, layer, sel_of(seqs), seqs.count, d_q, d_out, d_tok_mass_opt, cs),
+    st = cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
+                                       seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt, cs),
+                 "tensor-core attend");
+  } else {
+    st = cuda_ok(ctx, launch_attend_general(ctx->dev, layer, sel_of(seqs), seqs.count, d_q, d_out, d_tok_mass_opt, cs),
                  "attend");
+  }
+  return st;
 }
 
 kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_k, const void* d_v,
                              const void* d_q, float* d_out, float* d_tok_mass_opt, kvs_stream_t stream) {
+  Trace trace_("kvs_append_attend");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -625,16 +701,28 @@ kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
   if (!d_k || !d_v) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "NULL K or V");
   st = check_attend_buffers(ctx, d_q, d_out, d_tok_mass_opt);
   if (st != KVS_OK) return st;
-  if (ctx->kernel == KVS_KERNEL_TENSOR && ctx->plan.mode != KVS_MODE_H2O) {
+  if (ctx->kernel == KVS_KERNEL_TENSOR) {
     const int B = ctx->cfg.max_seqs;
     ctx->bounds.resize(ctx->sids.size());
+    bool lead = false;
     for (size_t i = 0; i < ctx->sids.size(); ++i) {
       const int32_t s = ctx->sids[i];
       const int64_t nx = ctx->next[(size_t)layer * B + s];
       if (nx + 1 > ctx->cfg.max_positions)
         return fail(ctx, KVS_ERR_CAPACITY, "sequence %d: position %lld + 1 exceeds max_positions %d", s,
                     (long long)nx, ctx->cfg.max_positions);
-      ctx->bounds[i] = (int32_t)seq_block_bound(ctx, s);
+      if (nx + 1 > ctx->frontier[s]) lead = true;
+      // H2O: a block the new token opens is counted from the launch on
+      const int64_t grow = (ctx->plan.mode == KVS_MODE_H2O && nx + 1 > ctx->frontier[s] && nx % kBlock == 0) ? 1 : 0;
+      ctx->bounds[i] = (int32_t)std::min<int64_t>(ctx->plan.max_blocks, seq_block_bound(ctx, s) + grow);
+    }
+    if (ctx->plan.mode == KVS_MODE_H2O && lead) {
+      // H2O: the pages of blocks the new tokens open come from the pool in a small
+      // launch of their own first (the fused kernel appends into existing pages)
+      st = cuda_ok(ctx, launch_alloc_pages(ctx->dev, layer, sel_of(seqs), seqs.count, 1,
+                                           reinterpret_cast<cudaStream_t>(stream)),
+                   "page allocation");
+      if (st != KVS_OK) return st;
     }
     AttendOpts opt;
     opt.k_new = d_k;
@@ -666,6 +754,7 @@ kvs_status kvs_append_attend(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
 kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const int32_t* d_block_ids,
                              int32_t ids_stride, const int32_t* d_block_count, const void* d_q, float* d_out,
                              kvs_stream_t stream) {
+  Trace trace_("kvs_attend_blocks");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -683,14 +772,16 @@ kvs_status kvs_attend_blocks(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const i
   opt.list_ids = d_block_ids;
   opt.list_count = d_block_count;
   opt.list_stride = ids_stride;
-  return cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
-                                       seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
-                                       reinterpret_cast<cudaStream_t>(stream)),
-                 "tensor-core block-list attend");
+  st = cuda_ok(ctx, launch_attend_tc(ctx->maps[2 * layer], ctx->maps[2 * layer + 1], ctx->dev, layer, sel_of(seqs),
+                                     seqs.count, d_q, d_out, ctx->bounds.data(), ctx->grid, opt,
+                                     reinterpret_cast<cudaStream_t>(stream)),
+               "tensor-core block-list attend");
+  return st;
 }
 
 kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q_obs, int32_t n_obs,
                              kvs_stream_t stream) {
+  Trace trace_("kvs_prefill_score");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -720,13 +811,15 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
                      ? kPrefillChunkMax
                      : (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, slots)));
   const int chunks = (int)cdiv64(maxb, cb);
-  return cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, sel_of(seqs), seqs.count, d_q_obs, n_obs, cb, chunks,
-                                           reinterpret_cast<cudaStream_t>(stream)),
-                 "prefill score");
+  st = cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, sel_of(seqs), seqs.count, d_q_obs, n_obs, cb, chunks,
+                                         reinterpret_cast<cudaStream_t>(stream)),
+               "prefill score");
+  return st;
 }
 
 kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q, float* d_out,
                                             float* d_tok_mass_opt, kvs_stream_t stream) {
+  Trace trace_("kvs_decode_attend_static_scratch");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   if (layer < 0 || layer >= ctx->cfg.num_layers) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "layer %d out of range", layer);
   kvs_status st = check_seqs(ctx, seqs);
@@ -746,26 +839,29 @@ kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer, kvs_seq
                                                 sel_of(seqs), seqs.count, d_q, d_out, d_tok_mass_opt,
                                                 ctx->bounds.data(), ctx->grid, reinterpret_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported)
-    return fail(ctx, KVS_ERR_UNSUPPORTED, "the logits of this launch do not fit in shared memory");
+    return fail(ctx, KVS_ERR_UNSUPPORTED, "the logits of this launch do not fit on chip");
   return cuda_ok(ctx, e, "tensor-core attend (library exchange area)");
 }
 
 
 kvs_status kvs_accumulate_scores(kvs_ctx* ctx, kvs_seqs seqs, kvs_stream_t stream) {
+  Trace trace_("kvs_accumulate_scores");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
   int64_t maxb = 1;
   st = accumulate_bounds(ctx, &maxb);
   if (st != KVS_OK) return st;
-  return cuda_ok(ctx, launch_accumulate(ctx->dev, sel_of(seqs), seqs.count, (int)maxb,
-                                        reinterpret_cast<cudaStream_t>(stream)),
-                 "accumulate");
+  st = cuda_ok(ctx, launch_accumulate(ctx->dev, sel_of(seqs), seqs.count, (int)maxb,
+                                      reinterpret_cast<cudaStream_t>(stream)),
+               "accumulate");
+  return st;
 }
 
 kvs_status kvs_select_blocks(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform,
                              int32_t score_kind, uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                              int32_t* d_keep_count, kvs_stream_t stream) {
+  Trace trace_("kvs_select_blocks");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
@@ -782,6 +878,7 @@ kvs_status kvs_select_blocks(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per
 kvs_status kvs_accumulate_select(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k_per_seq, int32_t k_uniform,
                                  int32_t score_kind, uint32_t flags, int32_t* d_keep_ids, int32_t keep_capacity,
                                  int32_t* d_keep_count, kvs_stream_t stream) {
+  Trace trace_("kvs_accumulate_select");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
@@ -807,6 +904,7 @@ kvs_status kvs_accumulate_select(kvs_ctx* ctx, kvs_seqs seqs, const int32_t* d_k
 
 kvs_status kvs_filter_blocks(kvs_ctx* ctx, kvs_seqs seqs, int32_t score_kind, double theta, int32_t* d_ids,
                              int32_t capacity, int32_t* d_count, kvs_stream_t stream) {
+  Trace trace_("kvs_filter_blocks");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   kvs_status st = check_seqs(ctx, seqs);
   if (st != KVS_OK) return st;
@@ -815,15 +913,17 @@ kvs_status kvs_filter_blocks(kvs_ctx* ctx, kvs_seqs seqs, int32_t score_kind, do
   if (theta != theta) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "theta is NaN");
   if (!d_ids || !d_count || capacity < 1)
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "output buffers missing or capacity < 1");
-  return cuda_ok(ctx, launch_filter(ctx->dev, sel_of(seqs), seqs.count, score_kind, theta, d_ids, capacity, d_count,
-                                    reinterpret_cast<cudaStream_t>(stream)),
-                 "filter");
+  st = cuda_ok(ctx, launch_filter(ctx->dev, sel_of(seqs), seqs.count, score_kind, theta, d_ids, capacity, d_count,
+                                  reinterpret_cast<cudaStream_t>(stream)),
+               "filter");
+  return st;
 }
 
 size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs) {
+  Trace trace_("kvs_scores_snapshot_bytes");
   if (!ctx || n_seqs < 0 || n_seqs > ctx->cfg.max_seqs) return 0;
-  void* ptr[11];
-  size_t bytes[11];
+  void* ptr[kSnapSections];
+  size_t bytes[kSnapSections];
   const int ns = snapshot_sections(ctx, 0, n_seqs, ptr, bytes);
   size_t total = 0;
   for (int i = 0; i < ns; ++i) total += round256(bytes[i]);
@@ -831,14 +931,17 @@ size_t kvs_scores_snapshot_bytes(const kvs_ctx* ctx, int32_t n_seqs) {
 }
 
 kvs_status kvs_export_scores(kvs_ctx* ctx, kvs_seqs seqs, void* dst, size_t dst_bytes, kvs_stream_t stream) {
+  Trace trace_("kvs_export_scores");
   return snapshot_copy(ctx, seqs, dst, dst_bytes, true, stream);
 }
 
 kvs_status kvs_import_scores(kvs_ctx* ctx, kvs_seqs seqs, const void* src, size_t src_bytes, kvs_stream_t stream) {
+  Trace trace_("kvs_import_scores");
   return snapshot_copy(ctx, seqs, const_cast<void*>(src), src_bytes, false, stream);
 }
 
 size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
+  Trace trace_("kvs_state_bytes");
   if (!ctx) return 0;
   const size_t slots = (size_t)ctx->plan.num_pages * kBlock, B = ctx->cfg.max_seqs, MB = ctx->plan.max_blocks;
   switch (what) {
@@ -854,12 +957,14 @@ size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what) {
     case KVS_STATE_BLOCK_TABLE: return B * MB * 4;
     case KVS_STATE_TRAJECTORY: return B * MB * (size_t)ctx->cfg.traj_len * 4;
     case KVS_STATE_LAYER_PROFILE: return B * MB * (size_t)ctx->dev.n_prof * 8;
+    case KVS_STATE_HEAD_PROFILE: return B * MB * (size_t)ctx->dev.n_hprof * 8;
     default: return 0;
   }
 }
 
 kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst, size_t dst_bytes,
                           kvs_stream_t stream) {
+  Trace trace_("kvs_read_state");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   const size_t n = kvs_state_bytes(ctx, what);
   if (n == 0) return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "state item %d not available", what);
@@ -884,6 +989,7 @@ kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst
     case KVS_STATE_STEPS: src = d.steps; break;
     case KVS_STATE_BLOCK_TABLE: src = d.block_table; break;
     case KVS_STATE_LAYER_PROFILE: src = d.prof; break;
+    case KVS_STATE_HEAD_PROFILE: src = d.hprof; break;
     case KVS_STATE_TRAJECTORY:
       return cuda_ok(ctx, launch_read_trajectory(d, static_cast<float*>(d_dst), cs), "read trajectory");
     case KVS_STATE_E_TOKEN: case KVS_STATE_E_BLOCK: case KVS_STATE_T_BLOCK:
@@ -894,6 +1000,7 @@ kvs_status kvs_read_state(kvs_ctx* ctx, int32_t what, int32_t layer, void* d_dst
 }
 
 kvs_status kvs_get_layout(const kvs_ctx* ctx, kvs_layout* out) {
+  Trace trace_("kvs_get_layout");
   if (!ctx || !out) return KVS_ERR_INVALID_ARGUMENT;
   std::memset(out, 0, sizeof *out);
   out->mode = ctx->plan.mode;
@@ -906,6 +1013,7 @@ kvs_status kvs_get_layout(const kvs_ctx* ctx, kvs_layout* out) {
 }
 
 kvs_status kvs_get_status(kvs_ctx* ctx, kvs_stream_t stream) {
+  Trace trace_("kvs_get_status");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   kvs_status st = cuda_ok(ctx, cudaStreamSynchronize(cs), "synchronise");
@@ -916,17 +1024,22 @@ kvs_status kvs_get_status(kvs_ctx* ctx, kvs_stream_t stream) {
   if (e & kErrTimeout) return fail(ctx, KVS_ERR_TIMEOUT, "a device-side wait ran out (error word 0x%x)", e);
   if (e & kErrCapacity) return fail(ctx, KVS_ERR_CAPACITY, "device capacity exhausted (error word 0x%x)", e);
   if (e & kErrState) return fail(ctx, KVS_ERR_STATE, "inconsistent device state (error word 0x%x)", e);
+  if (e & kErrBounds)
+    return fail(ctx, KVS_ERR_STATE, "a debug bounds check failed: an index read from device memory was out of "
+                                    "range (error word 0x%x)", e);
   return KVS_OK;
 }
 
 kvs_status kvs_clear_error(kvs_ctx* ctx, kvs_stream_t stream) {
+  Trace trace_("kvs_clear_error");
   if (!ctx) return KVS_ERR_INVALID_ARGUMENT;
   return cuda_ok(ctx, launch_clear(ctx->dev, reinterpret_cast<cudaStream_t>(stream)), "clear error");
 }
 
-const char* kvs_last_error(const kvs_ctx* ctx) { return ctx ? ctx->err.c_str() : ""; }
+const char* kvs_last_error(const kvs_ctx* ctx) { Trace trace_("kvs_last_error"); return ctx ? ctx->err.c_str() : ""; }
 
 const char* kvs_status_string(kvs_status s) {
+  Trace trace_("kvs_status_string");
   switch (s) {
     case KVS_OK: return "ok";
     case KVS_ERR_INVALID_ARGUMENT: return "invalid argument";
@@ -940,6 +1053,15 @@ const char* kvs_status_string(kvs_status s) {
   }
 }
 
-int32_t kvs_abi_version(void) { return KVS_ABI_VERSION; }
+uint32_t kvs_build_info(void) {
+  Trace trace_("kvs_build_info");
+  uint32_t f = tracing_on() ? KVS_BUILD_TRACING : 0u;
+#ifdef KVS_DEBUG
+  f |= KVS_BUILD_DEBUG_CHECKS;
+#endif
+  return f;
+}
+
+int32_t kvs_abi_version(void) { Trace trace_("kvs_abi_version"); return KVS_ABI_VERSION; }
 
 }  // extern "C"

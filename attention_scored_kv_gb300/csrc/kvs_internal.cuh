@@ -15,7 +15,8 @@
 //     score tables C/E per token [max_seqs][max_positions] double, stamp int32;
 //     C/E per block [max_seqs][max_blocks] double, stamp int32; steps [max_seqs] int32
 //     side-car: trajectory ring [max_seqs][max_blocks][traj_len] float, layer profiles
-//     [max_seqs][max_blocks][profiled layers] double
+//     [max_seqs][max_blocks][profiled layers] double, head profiles [max_seqs][max_blocks]
+//     [profiled heads] double and their per-step inputs [max_seqs][max_blocks][4] float
 //     attend partials: output rows [(grid_max + max_seqs)][Hq][D] float and (m, l) words
 //     [(grid_max + max_seqs)][Hq] u64; arrival counters
 //     logit scratch (the general kernel, and the tensor kernel when logits do not fit
@@ -39,6 +40,7 @@ enum : int32_t {
   kErrCapacity = 1,      // H2O page pool empty / position overflow seen on device
   kErrTimeout = 2,       // a bounded wait ran out
   kErrState = 4,         // missing page / inconsistent state seen on device
+  kErrBounds = 8,        // a debug-build bounds check failed (the access was skipped)
 };
 
 // The attend's per-sequence counters each sit on a 128-byte line of their own: every
@@ -97,6 +99,11 @@ struct Dev {
   float* traj;  int32_t traj_len;                    // [max_seqs][max_blocks][traj_len] ring of t_blk
   double* prof; int32_t n_prof;                      // [max_seqs][max_blocks][n_prof] layer profiles
   int32_t prof_layer[4];                             // profiled layers, ascending
+  // per-head profiles: the attend of layer hprof_layer[j] writes head hprof_head[j]'s
+  // in-block weight to hstep [max_seqs][max_blocks][4]; the accumulate adds it to
+  // hprof [max_seqs][max_blocks][n_hprof]
+  float* hstep; double* hprof; int32_t n_hprof;
+  int32_t hprof_layer[4], hprof_head[4];
   // prefill scoring scratch (obs_window > 0): row partials [max_seqs][chunks][Hq][32] and
   // statistics [max_seqs][Hq][32] as (max, sum) / (max, 1/sum); per KV head the entry
   // sums [max_seqs][Hkv][ps_bound][16] and block values [max_seqs][Hkv][ps_bound];
@@ -165,6 +172,24 @@ __device__ __forceinline__ int32_t block_at(const Dev& d, int s, const SeqBlocks
 }
 
 __device__ __forceinline__ void set_error(const Dev& d, int32_t bits) { atomicOr(d.err, bits); }
+
+// Debug builds (KVS_DEBUG) check indices that come from device memory the host could
+// not validate (sequence ids of a device list, pages, block ids) before using them: a
+// failed check records kErrBounds and the caller skips the access.  Release builds
+// compile the checks away.
+#ifdef KVS_DEBUG
+#define KVS_DCHECK(d, cond) ((cond) ? true : (set_error((d), kErrBounds), false))
+#else
+#define KVS_DCHECK(d, cond) true
+#endif
+
+// Per-head profiles: record head h's in-block weight w of block k of sequence s, when
+// (layer, h) is profiled.
+__device__ __forceinline__ void record_head(const Dev& d, int layer, int s, int32_t k, int h, float w) {
+  for (int j = 0; j < d.n_hprof; ++j)
+    if (d.hprof_layer[j] == layer && d.hprof_head[j] == h)
+      d.hstep[((size_t)s * d.max_blocks + k) * 4 + j] = w;
+}
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

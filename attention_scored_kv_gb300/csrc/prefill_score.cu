@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(PT<PASS>::THREADS, PT<PASS>::MINB) ps_tc_kerne
   float* votes = reinterpret_cast<float*>(base + kQBytes + P::KBYTES + sizeof(TcSmem));   // [8][nkeys]
   const Dev& d = A.d;
   const int chunk = blockIdx.x, kvh = blockIdx.y, sl = blockIdx.z, s = A.sel.at(sl);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const SeqBlocks sb = seq_blocks(d, A.layer, s);
   const Chunk ck = chunk_of(sb, chunk, A.chunk_blocks, PASS == 2);
@@ -514,7 +515,10 @@ __global__ void __launch_bounds__(PT<PASS>::THREADS, PT<PASS>::MINB) ps_tc_kerne
   __syncthreads();
   for (int b = tid; b < nblk; b += P::THREADS) {            // ... and its max over the heads
     float mx = 0.f;
-    for (int hl = 0; hl < kGq; ++hl) mx = fmaxf(mx, bsum[hl * nblk + b]);
+    for (int hl = 0; hl < kGq; ++hl) {
+      mx = fmaxf(mx, bsum[hl * nblk + b]);
+      record_head(d, A.layer, s, sm.blk[lo_halo + b], kvh * kGq + hl, bsum[hl * nblk + b]);   // head profiles
+    }
     d.ps_blk[gbase + ck.i0 + b] = mx;
   }
   __syncthreads();
@@ -554,7 +558,9 @@ __global__ void ps_combine_kernel(PSArgs A, int n_seqs) {
   const int idx = blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= n_seqs * d.Hq * kObs) return;
   const int sl = idx / (d.Hq * kObs), hr = idx % (d.Hq * kObs);
-  const SeqBlocks sb = seq_blocks(d, A.layer, A.sel.at(sl));
+  const int s = A.sel.at(sl);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
+  const SeqBlocks sb = seq_blocks(d, A.layer, s);
   const int used = min((sb.n + A.chunk_blocks - 1) / A.chunk_blocks, A.n_chunks);
   float M = -INFINITY, L = 0.f;
   for (int c = 0; c < used; ++c) {

@@ -66,7 +66,8 @@ __device__ __forceinline__ double block_entry_sum(double x) {
 // new cumulative score in *c_new and the new EMA in *e_new.  The token-sum score
 // (H2O) accumulates xsum, and the TOVA score is xsum.  Side-car views ("Context views
 // at marginal cost", Tier 1): the trajectory ring keeps xsum in slot step % traj_len,
-// and each profiled layer's sum gains that layer's block mass.
+// each profiled layer's sum gains that layer's block mass, and each profiled head's sum
+// gains that head's in-block weight of the step.
 __device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int32_t step, double xsum,
                                              double* c_new, double* e_new) {
   float y = 0.f;
@@ -84,6 +85,7 @@ __device__ __forceinline__ void update_block(const Dev& d, int s, int32_t k, int
   if (d.traj_len) d.traj[t * d.traj_len + step % d.traj_len] = (float)xsum;
   for (int i = 0; i < d.n_prof; ++i)
     d.prof[t * d.n_prof + i] += (double)d.blk_mass[(size_t)d.prof_layer[i] * d.blk_layer_elems + t];
+  for (int j = 0; j < d.n_hprof; ++j) d.hprof[t * d.n_hprof + j] += (double)d.hstep[t * 4 + j];
   d.last_blk[t] = step;
   *c_new = c;
   *e_new = e;

@@ -60,6 +60,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(Dev d, SeqSel sel, con
   int32_t* sid = reinterpret_cast<int32_t*>(skey + kSmemCap);        // [kSmemCap]
   int32_t* spage = sid + kSmemCap;                                   // [kSmemCap]
   const int sl = blockIdx.x, s = sel.at(sl);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int n = sb.n;
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(kThreads) filter_kernel(Dev d, SeqSel sel, int
                                                             int32_t* ids, int capacity, int32_t* count) {
   __shared__ SelShared sh;
   const int sl = blockIdx.x, s = sel.at(sl), tid = threadIdx.x;
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const SeqBlocks sb = seq_blocks(d, 0, s);
   const int32_t steps_now = d.steps[s];
   int before = 0;

@@ -25,6 +25,7 @@ __global__ void init_free_stack(Dev d) {
 // One CTA per sequence: empty it in every layer.
 __global__ void reset_kernel(Dev d, SeqSel sel) {
   const int s = sel.at(blockIdx.x);
+  if (!KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) return;
   const size_t pos_base = (size_t)s * d.max_positions;
   const size_t blk_base = (size_t)s * d.max_blocks;
   for (int64_t p = threadIdx.x; p < d.max_positions; p += blockDim.x) {
@@ -43,6 +44,8 @@ __global__ void reset_kernel(Dev d, SeqSel sel) {
     d.traj[blk_base * d.traj_len + i] = 0.f;
   for (size_t i = threadIdx.x; i < (size_t)d.max_blocks * d.n_prof; i += blockDim.x)
     d.prof[blk_base * d.n_prof + i] = 0.0;
+  for (size_t i = threadIdx.x; i < (size_t)d.max_blocks * d.n_hprof; i += blockDim.x)
+    d.hprof[blk_base * d.n_hprof + i] = 0.0;
   if (d.mode == KVS_MODE_H2O) {
     // return every page of the sequence to the pool and clear its slots
     const int n = d.res_count[s];

@@ -163,7 +163,10 @@ typedef struct {
                                 sum over steps of layer l's block mass (at most 4 bits) */
   int32_t obs_window;        /* SnapKV prefill scoring: the most observation queries one
                                 kvs_prefill_score call takes (1..32); 0 = off */
-  int32_t reserved_i[2];     /* must be 0 */
+  int32_t n_profile_heads;   /* side-car per-head profiles: 0..4 profiled query heads */
+  int32_t profile_heads[4];  /* each layer * 65536 + query head: keep, per block, the sum over
+                                steps of that head's in-block weight in that layer */
+  int32_t reserved_i;        /* must be 0 */
   double  h2o_recent_frac;   /* H2O: always keep the last frac * budget tokens (0.25) */
   double  ema_decay;         /* d in E <- d*E + (1-d)*x, in [0, 1) (0.9) */
   double  reserved_d[2];     /* must be 0 */
@@ -381,11 +384,11 @@ KVS_API kvs_status kvs_filter_blocks(kvs_ctx* ctx, kvs_seqs seqs, int32_t score_
 /* Score snapshot (the side-car kept next to the session's KV: "Context views at
  * marginal cost", Tier 1).  Export copies, for the sequences of `seqs` in the call's
  * order, every score table (token and block cumulative, EMA and update stamps,
- * token-sum and TOVA block scores, the trajectory ring, the layer profiles) and the
+ * token-sum and TOVA block scores, the trajectory ring, the layer and head profiles) and the
  * step counts into one buffer; import copies such a buffer back into as many
  * sequences (any range or list of the same count).  The
  * buffer is raw and carries no header: it can be imported only into a context created
- * with the same max_positions, traj_len and profile_layers (the KV entries and the
+ * with the same max_positions, traj_len, profile_layers and n_profile_heads (the KV entries and the
  * residency are not part of it).  The buffer may be device memory or host memory
  * (pinned memory keeps the copies asynchronous); it must hold
  * kvs_scores_snapshot_bytes(ctx, seqs.count) bytes.  One cudaMemcpyAsync per table on
@@ -418,7 +421,9 @@ typedef enum {
   KVS_STATE_TRAJECTORY = 16, /* [max_seqs][max_blocks][traj_len] float32, oldest step first,
                                 0 where the block was not updated (traj_len > 0) */
   KVS_STATE_LAYER_PROFILE = 17, /* [max_seqs][max_blocks][profiled layers, ascending] float64 */
-  KVS_STATE_COUNT = 18
+  KVS_STATE_HEAD_PROFILE = 18,  /* [max_seqs][max_blocks][n_profile_heads] float64, in
+                                   profile_heads order */
+  KVS_STATE_COUNT = 19
 } kvs_state_item;
 
 KVS_API size_t kvs_state_bytes(const kvs_ctx* ctx, int32_t what);
@@ -453,6 +458,14 @@ KVS_API const char* kvs_last_error(const kvs_ctx* ctx);
 KVS_API const char* kvs_status_string(kvs_status s);
 
 KVS_API int32_t kvs_abi_version(void);
+
+#define KVS_BUILD_DEBUG_CHECKS 1u  /* built with KVS_DEBUG: device-side bounds checks that
+                                      record KVS_ERR_STATE instead of touching memory out of
+                                      range, and scratch poisoned with NaN at kvs_create */
+#define KVS_BUILD_TRACING      2u  /* NVTX ranges around every call (environment variable
+                                      KVS_NVTX set to anything but "0") */
+/* How this library was built and what it emits (KVS_BUILD_* bits). */
+KVS_API uint32_t kvs_build_info(void);
 
 #ifdef __cplusplus
 }

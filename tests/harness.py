@@ -6,6 +6,8 @@ back (codes, scales, positions, masses, score tables, kept blocks) and compared 
 the oracle, position by position, at the tolerances stated in the check functions.
 """
 
+import ctypes
+
 import numpy as np
 import torch
 
@@ -18,8 +20,11 @@ SCORE_TOL = 1e-4                                       # absolute, masses and sc
 _FMT = {"f32": kvs.F32, "bf16": kvs.BF16, "e4m3": kvs.E4M3}
 
 
-def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_layers=(), obs_window=0):
+def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_layers=(), obs_window=0,
+                profile_heads=()):
+    heads = [l * 65536 + h for l, h in profile_heads] + [0] * (4 - len(profile_heads))
     return kvs.config_init(
+        n_profile_heads=len(profile_heads), profile_heads=(ctypes.c_int32 * 4)(*heads),
         obs_window=obs_window, traj_len=traj_len, profile_layers=sum(1 << l for l in profile_layers),
         num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads, head_dim=wl.head_dim,
         max_seqs=wl.batch, max_positions=wl.max_positions, window=wl.window, block_tokens=wl.block_tokens,
@@ -28,8 +33,8 @@ def make_config(wl, kernel=kvs.KERNEL_AUTO, spin_limit=0, traj_len=0, profile_la
         in_dtype=_FMT[wl.in_dtype], kernel=kernel, spin_limit=spin_limit)
 
 
-def make_oracle(wl, n, traj_len=0, profile_layers=()):
-    return OracleKV(traj_len=traj_len, profile_layers=tuple(profile_layers),num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
+def make_oracle(wl, n, traj_len=0, profile_layers=(), profile_heads=()):
+    return OracleKV(traj_len=traj_len, profile_layers=tuple(profile_layers), profile_heads=tuple(profile_heads),num_layers=wl.num_layers, num_q_heads=wl.num_q_heads, num_kv_heads=wl.num_kv_heads,
                     head_dim=wl.head_dim, num_seqs=n, max_positions=wl.max_positions, kv_format=wl.kv_format,
                     window=wl.window, h2o_budget_tokens=wl.h2o_budget_tokens,
                     h2o_sink_tokens=wl.h2o_sink_tokens, h2o_recent_frac=wl.h2o_recent_frac,
@@ -102,13 +107,15 @@ class Run:
     """One workload on the GPU, with the oracle tracking ``oracle_seqs``."""
 
     def __init__(self, wl, oracle_seqs=(0,), kernel=kvs.KERNEL_AUTO, device="cuda", spin_limit=0, fused=False,
-                 traj_len=0, profile_layers=(), obs_window=0):
+                 traj_len=0, profile_layers=(), obs_window=0, profile_heads=()):
         self.wl = wl
         self.fused = fused            # decode steps through append_attend (one call per layer)
         self.inp = workloads.Inputs(wl, device=device)
-        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit, traj_len, profile_layers, obs_window))
+        self.cache = kvs.KVCache(make_config(wl, kernel, spin_limit, traj_len, profile_layers, obs_window,
+                                             profile_heads))
         self.oseqs = list(oracle_seqs)
-        self.oracle = make_oracle(wl, len(self.oseqs), traj_len, profile_layers) if self.oseqs else None
+        self.oracle = (make_oracle(wl, len(self.oseqs), traj_len, profile_layers, profile_heads) if self.oseqs
+                       else None)
         self.lens = self.inp.prefill_lengths()
         self.step = 0
         self.last_out = {}

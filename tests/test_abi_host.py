@@ -86,7 +86,7 @@ def test_sidecar_workspace():
 
 def test_reserved_fields_must_be_zero():
     cfg = cfg35b()
-    cfg.reserved_i[1] = 1
+    cfg.reserved_i = 1
     assert kvs.validate_config(cfg)[0] == _abi.ERR_INVALID_ARGUMENT
 
 
@@ -128,3 +128,33 @@ def test_workspace_grows_with_format():
     sizes = [kvs.workspace_bytes(cfg35b(kv_dtype=dt, in_dtype=_abi.BF16 if dt != _abi.F32 else _abi.F32))
              for dt in (_abi.E4M3, _abi.BF16, _abi.F32)]
     assert sizes[0] < sizes[1] < sizes[2]
+
+
+def test_debug_library_exports_the_same_symbols_and_says_so():
+    """The KVS_DEBUG build (device bounds checks, poisoned scratch) is a second library
+    with the same entry points; kvs_build_info tells the two apart."""
+    names = declared_symbols()
+    dbg = ctypes.CDLL(_abi.LIB_DEBUG_PATH)
+    for n in names:
+        assert hasattr(dbg, n), n
+    dbg.kvs_build_info.restype = ctypes.c_uint32
+    rel = ctypes.CDLL(_abi.LIB_PATH)
+    rel.kvs_build_info.restype = ctypes.c_uint32
+    assert dbg.kvs_build_info() & 1 and not rel.kvs_build_info() & 1
+
+
+def test_nvtx_ranges_are_switched_on_by_the_environment():
+    """With KVS_NVTX=1 every call opens an NVTX range (no tool attached: no effect) and
+    kvs_build_info reports it; host-only calls behave as before."""
+    import subprocess
+    import sys
+    code = ("import attention_scored_kv_gb300 as kvs\n"
+            "lib = kvs.lib()\n"
+            "assert lib.kvs_build_info() & 2\n"
+            "cfg = kvs.config_init(num_layers=2, num_q_heads=8, num_kv_heads=1, head_dim=128)\n"
+            "assert kvs.validate_config(cfg)[0] == 0 and kvs.workspace_bytes(cfg) > 0\n"
+            "print('NVTX_OK')\n")
+    env = dict(os.environ, KVS_NVTX="1")
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and "NVTX_OK" in r.stdout, r.stderr
+    assert not kvs.lib().kvs_build_info() & 2

@@ -178,3 +178,54 @@ def test_snapshot_resume_matches_uninterrupted_run():
     for w in _SNAP_ITEMS:
         assert torch.equal(sa[w], sb[w]), w
     assert a.cache.get_status() == 0 and b.cache.get_status() == 0
+
+
+HEADS = ((0, 3), (1, 0), (1, 13), (0, 31))      # (layer, query head): four KV groups
+
+
+def _check_head_profiles(run, heads, rel=0.0):
+    wl, lay = run.wl, run.cache.layout()
+    got = run.cache.read_state(kvs.STATE_HEAD_PROFILE).cpu().numpy().view(np.float64)
+    got = got.reshape(wl.batch, lay.max_blocks, len(heads))
+    worst = 0.0
+    for i, s in enumerate(run.oseqs):
+        ref = run.oracle.scores[i].hprof            # [heads][blocks]
+        n = ref.shape[1]
+        worst = max(worst, float(np.max(np.abs(got[s, :n] - ref.T) / (harness.SCORE_TOL + rel * np.abs(ref.T)))))
+    assert worst <= 1.0, worst
+
+
+@pytest.mark.parametrize("name,fused,kernel", [("e4m3-window", True, kvs.KERNEL_TENSOR),
+                                               ("bf16", False, kvs.KERNEL_TENSOR),
+                                               ("e4m3-h2o", True, kvs.KERNEL_TENSOR),
+                                               ("bf16", False, kvs.KERNEL_GENERAL)])
+def test_head_profiles_against_oracle(name, fused, kernel):
+    """Per-head profiles ("Context views at marginal cost", Tier 1 views: "within head
+    H" of a retrieval-head subset) of four (layer, head) pairs, every step, through the
+    separate calls, the bench's fused step, the general kernel and H2O eviction."""
+    wl = dataclasses.replace(SMALL[name], steps=min(SMALL[name].steps, 9))
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kernel, fused=fused, profile_heads=HEADS)
+    run.prefill()
+    for t in range(wl.steps):
+        if fused:
+            run.decode_step(select=False, accumulate=False)
+            run.accumulate_select()
+        else:
+            run.decode_step(select=True)
+        _check_head_profiles(run, HEADS)
+    assert run.cache.get_status() == 0, run.cache.last_error()
+
+
+def test_head_profiles_after_snapkv_scoring():
+    """SnapKV prefill scoring as the first step: the profiled heads' pooled in-block votes
+    start the profiles, then decode steps add their weights."""
+    wl = dataclasses.replace(SMALL["e4m3-window"], steps=3)
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kvs.KERNEL_TENSOR, obs_window=32,
+                      profile_heads=HEADS)
+    run.prefill()
+    run.prefill_score(16, rel=1e-5)
+    _check_head_profiles(run, HEADS, rel=1e-5)         # pooled votes: the SnapKV bar
+    for t in range(wl.steps):
+        run.decode_step(select=False)
+        _check_head_profiles(run, HEADS, rel=1e-5)
+    assert run.cache.get_status() == 0, run.cache.last_error()
