@@ -1340,25 +1340,32 @@ bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window
   return true;
 }
 
-// Tensor map over one layer's pages viewed as [num_pages][Hkv][16][D] elements.
-cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype) {
-  // the driver entry point is looked up once; threads racing on the first lookup store
-  // the same pointer
+// The driver's cuTensorMapEncodeTiled, looked up once (threads racing on the first
+// lookup store the same pointer); null when the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::atomic<PFN_cuTensorMapEncodeTiled_v12000> encode_fn{nullptr};
   PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn.load(std::memory_order_acquire);
   if (!encode) {
     cudaDriverEntryPointQueryResult qr;
     void* fn = nullptr;
-    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
-    if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qr);
+    if (e != cudaSuccess || qr != cudaDriverEntryPointSuccess || !fn) return nullptr;
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     encode_fn.store(encode, std::memory_order_release);
   }
+  return encode;
+}
+
+// Tensor map over one layer's pages viewed as [num_pages][Hkv][16][D] elements; a box is
+// one 16-token block of box_heads KV heads (128 bytes of each row).
+cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype, int box_heads) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
   const bool fp8 = kv_dtype == KVS_E4M3;
   const int esz = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)kD, (cuuint64_t)kBlock, (cuuint64_t)Hkv, (cuuint64_t)num_pages};
   cuuint64_t strides[3] = {(cuuint64_t)kD * esz, (cuuint64_t)kBlock * kD * esz, (cuuint64_t)Hkv * kBlock * kD * esz};
-  cuuint32_t box[4] = {(cuuint32_t)(fp8 ? 128 : 64), (cuuint32_t)kBlock, (cuuint32_t)Hkv, 1};
+  cuuint32_t box[4] = {(cuuint32_t)(fp8 ? 128 : 64), (cuuint32_t)kBlock, (cuuint32_t)box_heads, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult res = encode(map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

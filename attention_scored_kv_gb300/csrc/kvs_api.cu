@@ -21,7 +21,7 @@
 
 namespace kvs {
 bool tc_supported(int Hq, int Hkv, int D, int kv_dtype, int in_dtype, int window, int mode);
-cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype);
+cudaError_t make_page_map(CUtensorMap* map, const void* base, int num_pages, int Hkv, int kv_dtype, int box_heads);
 cudaError_t launch_attend_tc(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& d, int layer,
                              SeqSel sel, int n_seqs, const void* q, float* out, const int32_t* bounds, int grid,
                              const AttendOpts& opt, cudaStream_t st);
@@ -70,8 +70,8 @@ struct Plan {
   size_t k_pages, v_pages, k_scales, v_scales, pos, tok_mass, blk_mass, next_pos, app_tickets;
   size_t block_table, res_blocks, res_pages, res_count, free_pages, free_top;
   size_t c_tok, e_tok, last_tok, c_blk, e_blk, last_blk, s_blk, t_blk, traj, prof, hstep, hprof, steps, acc_tickets;
-  size_t partials, part_ml, counters, logits, ps_part, ps_stat, ps_tok, ps_blk, ps_tickets, err;
-  int ps_bound = 0, ps_chunks = 0;
+  size_t partials, part_ml, counters, logits, ps_part, ps_tok, ps_blk, ps_ready, ps_done, ps_tickets, err;
+  int ps_bound = 0;
 };
 
 size_t esize(int dt) { return dt == KVS_F32 ? 4 : (dt == KVS_BF16 ? 2 : 1); }
@@ -220,16 +220,18 @@ void make_plan(const kvs_config* c, Plan* p) {
   p->part_ml = take(((size_t)kGridMax + B) * Hq * 8);
   p->counters = take((size_t)kCounterInts * B * 4);
   p->logits = take(p->logit_elems * 4);
-  // prefill scoring scratch: chunks of at least kPrefillChunkMin resident blocks
+  // prefill scoring scratch, for the at most kPsSeqMax sequences of one launch: row
+  // partials per (CTA + group) slot, per group the entry sums and block values, the
+  // group arrival and departure counters, per (sequence, block) the KV-head tickets
   const bool ps = c->obs_window > 0;
+  const size_t Bp = ps ? std::min<size_t>(B, (size_t)kPsSeqMax) : 0, Hkv = c->num_kv_heads;
   p->ps_bound = ps ? p->res_blocks_per_seq : 0;
-  p->ps_chunks = ps ? (int)cdiv64(p->ps_bound, kPrefillChunkMin) : 0;
-  const size_t Hkv = c->num_kv_heads;
-  p->ps_part = take(B * p->ps_chunks * Hq * 32 * 8);
-  p->ps_stat = take(ps ? B * Hq * 32 * 8 : 0);
-  p->ps_tok = take(B * Hkv * p->ps_bound * kBlock * 4);
-  p->ps_blk = take(B * Hkv * p->ps_bound * 4);
-  p->ps_tickets = take(B * p->ps_chunks * 4);
+  p->ps_part = take(ps ? ((size_t)kGridMax + Bp * Hkv) * 256 * 8 : 0);
+  p->ps_tok = take(Bp * Hkv * p->ps_bound * kBlock * 4);
+  p->ps_blk = take(Bp * Hkv * p->ps_bound * 4);
+  p->ps_ready = take(Bp * Hkv * 4);
+  p->ps_done = take(Bp * Hkv * 4);
+  p->ps_tickets = take(Bp * p->ps_bound * 4);
   p->err = take(4);
   p->total = o;
 }
@@ -248,6 +250,7 @@ struct kvs_ctx {
   std::vector<int32_t> sids;        // per-call scratch: the call's sequence ids, in order
   std::vector<uint8_t> seen;        // per-call scratch: repeated-id check [max_seqs]
   std::vector<CUtensorMap> maps;    // [L][2]
+  std::vector<CUtensorMap> ps_maps; // [L]: bf16 K pages, one KV head per box (prefill scoring)
   std::string err;
 };
 
@@ -557,9 +560,10 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   d.logit_scratch_elems = p.logit_elems;
   d.err = reinterpret_cast<int32_t*>(w + p.err);
   d.ps_part = reinterpret_cast<float2*>(w + p.ps_part);
-  d.ps_stat = reinterpret_cast<float2*>(w + p.ps_stat);
   d.ps_tok = reinterpret_cast<float*>(w + p.ps_tok);
   d.ps_blk = reinterpret_cast<float*>(w + p.ps_blk);
+  d.ps_ready = reinterpret_cast<int32_t*>(w + p.ps_ready);
+  d.ps_done = reinterpret_cast<int32_t*>(w + p.ps_done);
   d.ps_tickets = reinterpret_cast<int32_t*>(w + p.ps_tickets);
   d.ps_bound = p.ps_bound;
 
@@ -574,11 +578,22 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
     }
     ctx->maps.resize((size_t)cfg->num_layers * 2);
     for (int l = 0; l < cfg->num_layers; ++l) {
-      if (make_page_map(&ctx->maps[2 * l], d.k_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype) != cudaSuccess ||
-          make_page_map(&ctx->maps[2 * l + 1], d.v_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype) != cudaSuccess) {
+      if (make_page_map(&ctx->maps[2 * l], d.k_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype,
+                        d.Hkv) != cudaSuccess ||
+          make_page_map(&ctx->maps[2 * l + 1], d.v_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype,
+                        d.Hkv) != cudaSuccess) {
         delete ctx;
         return KVS_ERR_CUDA;
       }
+    }
+    if (cfg->obs_window > 0 && cfg->kv_dtype == KVS_BF16) {
+      ctx->ps_maps.resize((size_t)cfg->num_layers);
+      for (int l = 0; l < cfg->num_layers; ++l)
+        if (make_page_map(&ctx->ps_maps[l], d.k_pages + l * d.page_layer_bytes, p.num_pages, d.Hkv, d.kv_dtype, 1) !=
+            cudaSuccess) {
+          delete ctx;
+          return KVS_ERR_CUDA;
+        }
     }
   }
   ctx->next.assign((size_t)cfg->num_layers * cfg->max_seqs, 0);
@@ -594,7 +609,7 @@ kvs_status kvs_create(const kvs_config* cfg, void* d_workspace, size_t workspace
   // element then shows up as a non-finite result.
   {
     const size_t regions[][2] = {{p.tok_mass, p.blk_mass}, {p.blk_mass, p.next_pos}, {p.hstep, p.hprof},
-                                 {p.partials, p.counters}, {p.logits, p.ps_part}, {p.ps_part, p.ps_tickets}};
+                                 {p.partials, p.counters}, {p.logits, p.ps_part}, {p.ps_part, p.ps_ready}};
     for (const auto& r : regions)
       if (r[1] > r[0] && cudaMemsetAsync(w + r[0], 0xFF, r[1] - r[0], s) != cudaSuccess) {
         delete ctx;
@@ -793,7 +808,6 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
   if (!d_q_obs || (reinterpret_cast<uintptr_t>(d_q_obs) & 15))
     return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "q_obs must be a 16-byte aligned device pointer");
   const int B = ctx->cfg.max_seqs;
-  int64_t maxb = 1;
   for (const int32_t s : ctx->sids) {
     const int64_t nx = ctx->next[(size_t)layer * B + s];
     if (nx < n_obs)
@@ -801,17 +815,11 @@ kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const v
                   (long long)nx, layer);
     if (ctx->plan.mode == KVS_MODE_WINDOW && n_obs > ctx->cfg.window)
       return fail(ctx, KVS_ERR_INVALID_ARGUMENT, "n_obs exceeds the window");
-    maxb = std::max(maxb, seq_block_bound(ctx, s));
   }
-  maxb = std::min<int64_t>(maxb, ctx->plan.ps_bound);
-  // chunk size: the largest (fewest CTAs, least fixed cost per block) unless the launch
-  // would then leave SMs idle: two CTAs fit an SM
-  const int64_t units = maxb * seqs.count * ctx->cfg.num_kv_heads, slots = 2 * (int64_t)ctx->sm_count;
-  const int cb = units >= (int64_t)kPrefillChunkMax * slots
-                     ? kPrefillChunkMax
-                     : (int)std::min<int64_t>(kPrefillChunkMax, std::max<int64_t>(kPrefillChunkMin, cdiv64(units, slots)));
-  const int chunks = (int)cdiv64(maxb, cb);
-  st = cuda_ok(ctx, launch_prefill_score(ctx->dev, layer, sel_of(seqs), seqs.count, d_q_obs, n_obs, cb, chunks,
+  // one CTA per SM; calls of more than kPsSeqMax sequences run as several launches
+  const int grid = std::min(ctx->sm_count, kGridMax);
+  st = cuda_ok(ctx, launch_prefill_score(ctx->dev, ctx->ps_maps.empty() ? nullptr : &ctx->ps_maps[layer], layer,
+                                         sel_of(seqs), seqs.count, d_q_obs, n_obs, grid,
                                          reinterpret_cast<cudaStream_t>(stream)),
                "prefill score");
   return st;

@@ -33,7 +33,7 @@ namespace kvs {
 
 constexpr int kBlock = 16;          // tokens per block (placement unit)
 constexpr int kGridMax = 256;       // upper bound of persistent attend CTAs (sizing)
-constexpr int kPrefillChunkMin = 16, kPrefillChunkMax = 32;   // blocks per prefill-scoring CTA
+constexpr int kPsSeqMax = 512;     // sequences of one prefill-scoring launch
 
 // Device error word bits.
 enum : int32_t {
@@ -104,11 +104,13 @@ struct Dev {
   // hprof [max_seqs][max_blocks][n_hprof]
   float* hstep; double* hprof; int32_t n_hprof;
   int32_t hprof_layer[4], hprof_head[4];
-  // prefill scoring scratch (obs_window > 0): row partials [max_seqs][chunks][Hq][32] and
-  // statistics [max_seqs][Hq][32] as (max, sum) / (max, 1/sum); per KV head the entry
-  // sums [max_seqs][Hkv][ps_bound][16] and block values [max_seqs][Hkv][ps_bound];
-  // tickets [max_seqs][chunks]
-  float2* ps_part; float2* ps_stat; float* ps_tok; float* ps_blk; int32_t* ps_tickets;
+  // prefill scoring scratch (obs_window > 0), for the S <= kPsSeqMax sequences of one
+  // launch and its groups g = (launch slot, KV head): row partials (max, sum) per (CTA +
+  // group) slot [kGridMax + S * Hkv][256]; per group the entry sums [S * Hkv][ps_bound][16]
+  // and block values [S * Hkv][ps_bound]; group arrival and departure counters
+  // [S * Hkv]; KV-head tickets [S][ps_bound]
+  float2* ps_part; float* ps_tok; float* ps_blk;
+  int32_t* ps_ready; int32_t* ps_done; int32_t* ps_tickets;
   int32_t ps_bound;
   int32_t* steps;                                    // [max_seqs]
   int32_t* acc_tickets;                              // [max_seqs]
@@ -258,7 +260,11 @@ cudaError_t launch_filter(const Dev& d, SeqSel sel, int n_seqs, int score_kind, 
                           int capacity, int32_t* count, cudaStream_t st);
 cudaError_t launch_clear(const Dev& d, cudaStream_t st);
 int prefill_obs_max();
-cudaError_t launch_prefill_score(const Dev& d, int layer, SeqSel sel, int n_seqs, const void* q_obs, int n_obs,
-                                 int chunk_blocks, int n_chunks, cudaStream_t st);
+}  // namespace kvs
+struct CUtensorMap_st;
+namespace kvs {
+// k_map: the layer's bf16 K pages with one KV head per box (null for E4M3 caches)
+cudaError_t launch_prefill_score(const Dev& d, const CUtensorMap_st* k_map, int layer, SeqSel sel, int n_seqs,
+                                 const void* q_obs, int n_obs, int grid, cudaStream_t st);
 size_t general_smem_bytes(int Hq, int D);
 }  // namespace kvs

@@ -275,11 +275,11 @@ def run_ours(args, world, rank, local):
         res_blocks = (wl.window // 16 + 1) if wl.window else lay.max_blocks
         k_sel, flags = wl0.keep_k(res_blocks), 0
     launches = {"n": 0}
-    # append + attend is one launch per layer with the tensor-core attend outside H2O mode
-    # when every sequence can have CTAs of its own; otherwise append and attend are two,
-    # and H2O adds one page allocation per step (the first layer to reach a new position).
-    # accumulate + select is one launch up to 512 resident blocks per sequence.
-    fused = lay.attend_kernel == kvs.KERNEL_TENSOR and not wl.h2o_budget_tokens and B <= lay.attend_grid
+    # append + attend is one launch per layer with the tensor-core attend when every
+    # sequence can have CTAs of its own; otherwise append and attend are two.  H2O adds
+    # one page allocation per step (the first layer to reach a new position).  accumulate
+    # + select is one launch up to 512 resident blocks per sequence.
+    fused = lay.attend_kernel == kvs.KERNEL_TENSOR and B <= lay.attend_grid
     res_bound = (wl.window // 16 + 1) if wl.window else (
         wl.h2o_budget_tokens // 16 + 2 if wl.h2o_budget_tokens else lay.max_blocks)
     per_step_launches = ((L if fused else 2 * L) + (1 if res_bound <= 512 else 2)
@@ -392,8 +392,8 @@ def run_ours(args, world, rank, local):
         reattend = {"blocks_kept": kept, "kv_bytes_per_launch": int(rbytes), "launch_us": round(reattend_us, 3),
                     "kv_gbs": round(rbytes / (reattend_us * 1e-6) / 1e9, 1),
                     "frac_of_hbm": round(rbytes / (reattend_us * 1e-6) / 1e9 / hbm, 4)}
-    # ---- SnapKV prefill scoring of every layer over the current cache (three launches
-    # per layer), graph of L layers; FLOPs = QK^T of the observation queries once
+    # ---- SnapKV prefill scoring of every layer over the current cache (one launch per
+    # layer), graph of L layers; FLOPs = QK^T of the observation queries once
     prefill_score = None
     if cache.cfg.obs_window:
         QO = torch.stack([inp.obs_q(l, OBS_WINDOW) for l in range(L)])
@@ -415,7 +415,7 @@ def run_ours(args, world, rank, local):
         qk_flops = 2.0 * OBS_WINDOW * Hq * entries * D
         peak_tf, tf_kind = bf16_peak()
         tf = qk_flops / (ps_us * 1e-6) / 1e12
-        prefill_score = {"n_obs": OBS_WINDOW, "layer_us": round(ps_us, 3), "launches_per_layer": 3,
+        prefill_score = {"n_obs": OBS_WINDOW, "layer_us": round(ps_us, 3), "launches_per_layer": 1,
                          "qk_flops_per_layer": int(qk_flops), "tflops": round(tf, 1),
                          "tflops_executed": round(2 * tf, 1), "peak_tflops": peak_tf, "peak_source": tf_kind,
                          "frac": round(tf / peak_tf, 4), "frac_executed": round(2 * tf / peak_tf, 4),
