@@ -33,9 +33,9 @@
 //   * The KV heads of a block meet last: each group's entry sums and block values go to
 //     global memory, a per-block ticket counts the KV heads, and the last arrival sums
 //     the entries in KV-head order and takes the block maximum.
-//   * Roles: a producer warp (TMA copies, block lists), an MMA warp (one thread issues
-//     tcgen05.mma and commits to mbarriers), a statistics warp and sixteen epilogue
-//     warps.  For E4M3 caches the epilogue warps also decode stage s + 1's codes to f16
+//   * Roles: a producer warp (key copies, block lists), an MMA warp (one thread issues
+//     tcgen05.mma, commits to mbarriers, and copies a new group's queries once the old
+//     ones' MMAs are done), a statistics warp and sixteen epilogue warps.  For E4M3 caches the epilogue warps also decode stage s + 1's codes to f16
 //     (exact) into the swizzled operand tile while stage s's MMAs run, and round a new
 //     group's queries to f16 (exact in f16's normal range).  Both phases stream the
 //     keys, so the layer's keys are read from HBM once and from L2 the second time.
@@ -71,7 +71,10 @@ constexpr int kInfo = 8;                               // stage-info ring
 constexpr int kScRing = 4;                             // E4M3 key-scale ring
 constexpr int kPieceList = 64;                         // pieces whose tickets wait for the end
 static_assert(2 * kPieceList * kPieceMax <= kGq * kVoteKeys, "the winner list lives in the votes buffer");
-constexpr int kMbarLimit = 1 << 22;                    // polls of an mbarrier before giving up
+// An mbarrier poll suspends the thread until the phase completes or kSuspendNs pass, so
+// a waiting warp takes no issue slots; kMbarLimit polls (about a second) bound a wait.
+constexpr uint32_t kSuspendNs = 2000;
+constexpr int kMbarLimit = 1 << 19;
 constexpr float kLog2e = 1.4426950408889634f;
 
 constexpr int kEpiWarps = 16, kEpiThreads = kEpiWarps * 32;
@@ -130,8 +133,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 }
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-               : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+               " selp.u32 %0, 1, 0, p;\n}\n"
+               : "=r"(ok) : "r"(bar), "r"(parity), "n"(kSuspendNs) : "memory");
   return ok != 0;
 }
 // Bounded wait for the phase with the given parity.  A wait that runs out records
@@ -141,7 +145,7 @@ __device__ __forceinline__ bool mbar_wait(const Dev& d, PsShared& sm, const uint
   const uint32_t bar = smem_u32(&b);
   for (int it = 0; it < kMbarLimit; ++it) {
     if (mbar_test(bar, parity)) return true;
-    if ((it & 255) == 255 && *reinterpret_cast<volatile int32_t*>(&sm.abort)) return false;
+    if ((it & 15) == 15 && *reinterpret_cast<volatile int32_t*>(&sm.abort)) return false;
   }
   *reinterpret_cast<volatile int32_t*>(&sm.abort) = 1;
   set_error(d, kErrTimeout);
@@ -226,10 +230,11 @@ __device__ __forceinline__ float sum_ex2(const float (&v)[32], float c, float o)
   }
   return (acc[0].x + acc[0].y) + (acc[1].x + acc[1].y);
 }
-__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
-  uint32_t r;
-  const uint16_t a = (uint16_t)two;
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(a));
+// Four E4M3 codes (one 32-bit word) to four f16 (two words), exact.
+__device__ __forceinline__ uint2 e4m3x4_f16x4(uint32_t w) {
+  uint2 r;
+  asm("{\n .reg .b16 lo, hi;\n mov.b32 {lo, hi}, %2;\n cvt.rn.f16x2.e4m3x2 %0, lo;\n cvt.rn.f16x2.e4m3x2 %1, hi;\n}"
+      : "=r"(r.x), "=r"(r.y) : "r"(w));
   return r;
 }
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w) {
@@ -450,7 +455,7 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
     Sched S;
     S.init(sm.seq_off, A.n_seqs, d.Hkv, x0, x1);
     Stage st;
-    int s = 0, qn = 0, cur = -1, sid = 0;
+    int s = 0, cur = -1, sid = 0;
     SeqBlocks sb{};
     const uint8_t* kl = d.k_pages + (size_t)A.layer * d.page_layer_bytes;
     const float* kscl = FP8 ? d.k_scales + (size_t)A.layer * d.slot_layer_elems : nullptr;
@@ -502,19 +507,6 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
                         st.kvh, page, bar);
         }
       }
-      // a new group's queries, once the old ones' MMAs are done
-      if (st.new_q) {
-        if (lane == 0) {
-          if (qn > 0) mbar_wait(d, sm, sm.qfree, (qn - 1) & 1);
-          mbar_expect_tx(smem_u32(&sm.qfull), 2u * kGq * A.n_obs * 128u);
-          for (int kh = 0; kh < 2; ++kh)
-            for (int hl = 0; hl < kGq; ++hl)
-              tma_load_4d(smem_u32(qt + kh * kQHalf + hl * kObs * 128), &tq, 64 * kh, st.kvh * kGq + hl, 0, st.sl,
-                          smem_u32(&sm.qfull));
-        }
-        __syncwarp();
-        ++qn;
-      }
       ++s;
     }
   } else if (warp == kMmaWarp) {
@@ -527,7 +519,17 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
       const uint32_t qs = smem_u32(qt), ts = smem_u32(tiles);
       while (S.next(st)) {
         if (st.new_q) {
-          if (qn > 0) umma::commit(smem_u32(&sm.qfree));
+          // a new group's queries: once the old ones' MMAs are done, this thread copies
+          // them (the producer keeps streaming keys meanwhile)
+          if (qn > 0) {
+            umma::commit(smem_u32(&sm.qfree));
+            mbar_wait(d, sm, sm.qfree, (qn - 1) & 1);
+          }
+          mbar_expect_tx(smem_u32(&sm.qfull), 2u * kGq * A.n_obs * 128u);
+          for (int kh = 0; kh < 2; ++kh)
+            for (int hl = 0; hl < kGq; ++hl)
+              tma_load_4d(smem_u32(qt + kh * kQHalf + hl * kObs * 128), &tq, 64 * kh, st.kvh * kGq + hl, 0, st.sl,
+                          smem_u32(&sm.qfull));
           mbar_wait(d, sm, FP8 ? sm.qready : sm.qfull, qn & 1);
           ++qn;
         }
@@ -614,6 +616,13 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
     int64_t obs0 = 0;
     float m_run = -INFINITY, l_run = 0.f;
     const float cs = FP8 ? 1.f : qk_scale;   // bf16: the logits stay raw until the exponent
+    // E4M3: the thread decodes codes 16 c16 .. 16 c16 + 15 of keys dk_key and dk_key + 64
+    // (c16 = tid % 8); their places in the raw copy and in the swizzled tile are the same
+    // every stage
+    const int dk_key = tid >> 3, dk_c16 = tid & 7;
+    const int dk_src = dk_key * kD + dk_c16 * 16;
+    const int dk_dst = (int)umma::sw128_offset(kSK, dk_key, 16 * dk_c16);
+    const int dk_dst8 = (int)umma::sw128_offset(kSK, dk_key, 16 * dk_c16 + 8);
     // E4M3: this thread's share of stage j's decode (codes to f16 in the swizzled tile
     // j % 2, scales x log2(e)/sqrt(D) to the ring); returns whether stage j starts a
     // group.  Tile j % 2 is free: this warp waited for stage j - 2's MMAs one stage ago.
@@ -625,15 +634,13 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
       mbar_wait(d, sm, sm.kfull[slot], (j / C::NR) & 1);
       const uint8_t* rw = raws + slot * kRawBytes;
       uint8_t* kt = tiles + (j % C::NK) * kTileBytes;
-      for (int i = tid; i < nb * kBlock * 8; i += kEpiThreads) {   // 16 codes each
-        const int key = i >> 3, c16 = i & 7;
-        const uint4 cw = *reinterpret_cast<const uint4*>(rw + key * kD + c16 * 16);
-        const uint4 lo = make_uint4(e4m3x2_f16x2(cw.x & 0xffffu), e4m3x2_f16x2(cw.x >> 16),
-                                    e4m3x2_f16x2(cw.y & 0xffffu), e4m3x2_f16x2(cw.y >> 16));
-        const uint4 hi = make_uint4(e4m3x2_f16x2(cw.z & 0xffffu), e4m3x2_f16x2(cw.z >> 16),
-                                    e4m3x2_f16x2(cw.w & 0xffffu), e4m3x2_f16x2(cw.w >> 16));
-        sts128(kt + umma::sw128_offset(kSK, key, 16 * c16), lo);
-        sts128(kt + umma::sw128_offset(kSK, key, 16 * c16 + 8), hi);
+#pragma unroll
+      for (int h2 = 0; h2 < 2; ++h2) {                // keys dk_key and dk_key + 64
+        if (dk_key + 64 * h2 >= nb * kBlock) break;
+        const uint4 cw = *reinterpret_cast<const uint4*>(rw + dk_src + h2 * 64 * kD);
+        const uint2 a = e4m3x4_f16x4(cw.x), b = e4m3x4_f16x4(cw.y), c2 = e4m3x4_f16x4(cw.z), e = e4m3x4_f16x4(cw.w);
+        sts128(kt + dk_dst + h2 * 64 * 128, make_uint4(a.x, a.y, b.x, b.y));
+        sts128(kt + dk_dst8 + h2 * 64 * 128, make_uint4(c2.x, c2.y, e.x, e.y));
       }
       if (tid < kSK) sm.sc[j % kScRing][tid] = tid < nb * kBlock ? sm.sc_raw[slot][tid] * qk_scale : 0.f;
       umma::fence_async_smem();
@@ -808,60 +815,77 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
           // block are consecutive; across blocks they are when the next streamed block is
           // the next block id.  A key that is not resident has vote 0, so it can sit in a
           // max without changing it, but its own pooled value is 0.
-          const int c0 = I.c0, c1 = I.c1, nstream = I.b0 + nb - I.v0, lo_halo = c0 - I.v0, nck = (c1 - c0) * kBlock;
+          const int c0 = I.c0, c1 = I.c1, nstream = I.b0 + nb - I.v0, lo_halo = c0 - I.v0, nblk = c1 - c0;
           const int g = I.sl * d.Hkv + I.kvh;
           const size_t gbase = (size_t)g * d.ps_bound + c0;
-          for (int base = 0; base < nck; base += kEpiThreads) {
-            const int item = base + tid;
-            const bool live = item < nck;
-            const int j = lo_halo * kBlock + item, b = j >> 4, cc = j & 15;
-            float pv[kGq];
+          // thread = (own block b = tid / 8, head hl = tid % 8): the block's 16 votes and 3
+          // on each side (0 where the neighbouring block is not the adjacent block id)
+          // in registers, the 16 pooled values, their sum; the 8 heads of a block are 8
+          // consecutive lanes, which reduce the block value (max) and the entry sums
+          static_assert(kEpiThreads >= kGq * kPieceMax, "one thread per (head, block) of a piece");
+          const int hl = tid & 7, b = tid >> 3;
+          const bool live = b < nblk;
+          const int sb_i = lo_halo + b;                    // streamed block index
+          float pooled[kBlock];
 #pragma unroll
-            for (int hl = 0; hl < kGq; ++hl) pv[hl] = 0.f;
-            if (live) {
-              const int64_t pj = (int64_t)sm.pblk[b] * kBlock + cc;
-              if (pj >= sb.lo && pj < sb.next) {
-                const bool prev = b > 0 && sm.pblk[b - 1] == sm.pblk[b] - 1;
-                const bool next = b + 1 < nstream && sm.pblk[b + 1] == sm.pblk[b] + 1;
-                const int lo = cc >= kPool || prev ? j - kPool : j - cc;
-                const int hi = cc + kPool < kBlock || next ? j + kPool : j - cc + kBlock - 1;
-                const int a0 = max(lo, 0), a1 = min(hi, nstream * kBlock - 1);
-                // seven taps, clamped into [a0, a1] (a clamped tap repeats one inside)
+          for (int cc = 0; cc < kBlock; ++cc) pooled[cc] = 0.f;
+          float bsum = 0.f;
+          int32_t blk = 0;
+          if (live) {
+            blk = sm.pblk[sb_i];
+            const bool prev = sb_i > 0 && sm.pblk[sb_i - 1] == blk - 1;
+            const bool next = sb_i + 1 < nstream && sm.pblk[sb_i + 1] == blk + 1;
+            const float* vr = votes + hl * kVoteKeys + sb_i * kBlock;
+            float w[kBlock + 2 * kPool];
 #pragma unroll
-                for (int hl = 0; hl < kGq; ++hl) {
-                  const float* vr = votes + hl * kVoteKeys;
-                  float m = vr[j];
-#pragma unroll
-                  for (int k = -kPool; k <= kPool; ++k) m = fmaxf(m, vr[min(max(j + k, a0), a1)]);
-                  pv[hl] = m;
-                }
-              }
+            for (int k = 0; k < kPool; ++k) {
+              w[k] = prev ? vr[k - kPool] : 0.f;
+              w[kBlock + kPool + k] = next ? vr[kBlock + k] : 0.f;
             }
-            float tsum = 0.f;
 #pragma unroll
-            for (int hl = 0; hl < kGq; ++hl) tsum += pv[hl];
-            if (live) d.ps_tok[gbase * kBlock + item] = tsum;
-            // per head the in-block sum over the 16 lanes of a block, and its max over heads
+            for (int cc = 0; cc < kBlock; ++cc) w[kPool + cc] = vr[cc];
+            const int64_t p0 = (int64_t)blk * kBlock;
 #pragma unroll
-            for (int hl = 0; hl < kGq; ++hl) {
-              float x = pv[hl];
-              x += __shfl_xor_sync(0xffffffffu, x, 8);
-              x += __shfl_xor_sync(0xffffffffu, x, 4);
-              x += __shfl_xor_sync(0xffffffffu, x, 2);
-              x += __shfl_xor_sync(0xffffffffu, x, 1);
-              pv[hl] = x;
+            for (int cc = 0; cc < kBlock; ++cc) {
+              const bool res = p0 + cc >= sb.lo && p0 + cc < sb.next;
+              const float m = max3(max3(w[cc], w[cc + 1], w[cc + 2]), max3(w[cc + 3], w[cc + 4], w[cc + 5]), w[cc + 6]);
+              pooled[cc] = res ? m : 0.f;
+              bsum += pooled[cc];
             }
-            if (live && (item & 15) == 0) {
-              const int bi = item >> 4;
-              const int32_t blk = sm.pblk[lo_halo + bi];
-              float mx = 0.f;
+          }
+          float mx = bsum;
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          // entry sums over the 8 heads: a reduce-scatter over the block's 8 lanes leaves
+          // lane hl with entries e0 = 8 bit2(hl) + 4 bit1(hl) + 2 bit0(hl) and e0 + 1
 #pragma unroll
-              for (int hl = 0; hl < kGq; ++hl) {
-                mx = fmaxf(mx, pv[hl]);
-                record_head(d, A.layer, sid, blk, I.kvh * kGq + hl, pv[hl]);   // head profiles
-              }
-              d.ps_blk[gbase + bi] = mx;
-            }
+          for (int k = 0; k < 8; ++k) {
+            const bool up = (hl & 4) != 0;
+            const float give = up ? pooled[k] : pooled[k + 8];
+            const float got = __shfl_xor_sync(0xffffffffu, give, 4);
+            pooled[k] = (up ? pooled[k + 8] : pooled[k]) + got;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const bool up = (hl & 2) != 0;
+            const float give = up ? pooled[k] : pooled[k + 4];
+            const float got = __shfl_xor_sync(0xffffffffu, give, 2);
+            pooled[k] = (up ? pooled[k + 4] : pooled[k]) + got;
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const bool up = (hl & 1) != 0;
+            const float give = up ? pooled[k] : pooled[k + 2];
+            const float got = __shfl_xor_sync(0xffffffffu, give, 1);
+            pooled[k] = (up ? pooled[k + 2] : pooled[k]) + got;
+          }
+          if (live) {
+            const int e0 = 8 * ((hl >> 2) & 1) + 4 * ((hl >> 1) & 1) + 2 * (hl & 1);
+            d.ps_tok[(gbase + b) * kBlock + e0] = pooled[0];
+            d.ps_tok[(gbase + b) * kBlock + e0 + 1] = pooled[1];
+            record_head(d, A.layer, sid, blk, I.kvh * kGq + hl, bsum);   // head profiles
+            if (hl == 0) d.ps_blk[gbase + b] = mx;
           }
           if (tid == 0) {
             const int k = sm.n_pieces;
