@@ -1283,9 +1283,12 @@ cudaError_t launch_one(const CUtensorMap& tk, const CUtensorMap& tv, const Dev& 
   return cudaLaunchKernelEx(&cfg, fn, tk, tv, d, P);
 }
 
-// Per-CTA block capacity a whole-CTA plan may use: up to an eighth more blocks than an
-// even split, plus two.
-int wide_cap(int base) { return base + base / 8 + 2; }
+// Per-CTA block capacity a whole-CTA plan may use: up to a quarter more blocks than an
+// even split, plus two.  (A batch of many sequences that each need a little more than
+// two even shares, such as 64 sequences of 130 blocks on 152 CTAs, then gets two CTAs
+// per sequence in a whole-CTA plan instead of the device split: measured 9 % faster per
+// attend, and the append joins the launch.)
+int wide_cap(int base) { return base + base / 4 + 2; }
 
 // Whole CTAs per sequence, planned on the host from the per-sequence block bounds: the
 // fewest blocks per CTA X <= cap_limit such that ceil(bound_b / X) CTAs for every
