@@ -73,6 +73,16 @@ def test_prefill_score_fullsize_e4m3_b16_ctx32768_window4096():
     _snap_run(wl, 32, [0, 9], steps=1)
 
 
+def test_prefill_score_over_more_sequences_than_one_launch_takes():
+    """A call of 530 sequences runs as launches of at most 512 (one launch's scoring
+    scratch holds 512 sequences).  Ragged short prompts of 2 to 6 blocks (no eviction
+    at this budget) put many (sequence, KV head) groups into each CTA's share;
+    sequences on both sides of the split follow the oracle."""
+    wl = workloads.scaled_down("e4m3-b64-ragged-h2o2048", name="snap-530", num_layers=1, batch=530,
+                               context_range=(40, 90), h2o_budget_tokens=256, steps=1, prefill_chunk=0)
+    _snap_run(wl, 32, [0, 1, 511, 512, 529], steps=1)
+
+
 def test_prefill_score_is_deterministic_and_leaves_the_cache():
     """Two calls give the same bytes; the K/V storage and positions are untouched."""
     wl = SMALL["e4m3-window"]
