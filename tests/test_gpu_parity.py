@@ -279,6 +279,69 @@ def test_attend_blocks_reports_a_bad_block_id():
     assert run.cache.get_status() == 0
 
 
+def _many(name, batch, **changes):
+    """SMALL[name] with more sequences: forty, more than a CTA each."""
+    wl = SMALL[name]
+    return workloads.scaled_down(wl.name.replace("-small", ""), **{**_fields(wl), "batch": batch, **changes})
+
+
+@pytest.mark.parametrize("name", ["bf16", "bf16-hkv8", "e4m3-window", "e4m3-h2o"])
+def test_attend_blocks_many_sequences_against_oracle(name):
+    """Tier-2 re-attend with 40 sequences against the oracle on three of them."""
+    wl = _many(name, 40, steps=3)
+    run = harness.Run(wl, oracle_seqs=[0, 17, 39], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    for t in range(wl.steps - 1):
+        run.decode_step(select=False)
+        run.select()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ncand = run.candidate_counts() if not wl.h2o_budget_tokens else [lay.max_blocks] * wl.batch
+    ks = torch.tensor([max(1, wl.keep_k(int(n)) // 2) for n in ncand], dtype=torch.int32, device="cuda")
+    ids, cnt = run.cache.select_blocks(ks, keep_capacity=lay.max_blocks)
+    worst, moved = _reattend_check(run, ids, cnt, t_query=wl.steps)
+    assert worst <= harness.OUT_TOL[wl.kv_format], worst
+    assert moved > 0.0
+    assert run.cache.get_status() == 0, run.cache.last_error()
+
+
+def test_attend_blocks_long_lists_many_sequences():
+    """Lists of 107 blocks, 40 sequences: every block kept equals full attention, and
+    the oracle agrees."""
+    wl = _many("e4m3-nowindow", 40, context=1700, steps=2)
+    run = harness.Run(wl, oracle_seqs=[0, 39], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ids, cnt = run.cache.select_blocks(10 ** 6, keep_capacity=lay.max_blocks)   # keeps all
+    assert int(cnt.min()) > 100
+    worst, _ = _reattend_check(run, ids, cnt, t_query=7)
+    assert worst <= harness.OUT_TOL[wl.kv_format], worst
+    for l in range(wl.num_layers):
+        q = run.inp.step_q(l, 9)
+        full = run.cache.decode_attend(l, q)
+        got = run.cache.attend_blocks(l, q, ids, cnt)
+        for b in range(wl.batch):                 # both within the bar of the oracle
+            err = harness.rel_err_rows(got[b].double().cpu().numpy(), full[b].double().cpu().numpy())
+            assert err <= 2 * harness.OUT_TOL[wl.kv_format], (b, err)
+    assert run.cache.get_status() == 0, run.cache.last_error()
+
+
+def test_attend_blocks_many_sequences_reports_a_bad_block_id():
+    wl = _many("e4m3-window", 40, steps=2)
+    run = harness.Run(wl, oracle_seqs=[], kernel=kvs.KERNEL_TENSOR)
+    run.prefill()
+    run.decode_step(select=False)
+    lay = run.cache.layout()
+    ids, cnt = run.cache.select_blocks(4, keep_capacity=lay.max_blocks)
+    bad = ids.clone()
+    bad[3, 1] = lay.max_blocks + 7                # out of range: reported, left out
+    run.cache.attend_blocks(0, run.inp.step_q(0, 5), bad, cnt)
+    assert run.cache.get_status() == kvs._abi.ERR_STATE
+    run.cache.clear_error()
+    assert run.cache.get_status() == 0
+
+
 @pytest.mark.parametrize("name", ["bf16", "e4m3-window", "e4m3-h2o"])
 def test_general_kernel_on_tensor_shapes(name):
     wl = SMALL[name]
