@@ -684,7 +684,7 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
         sb = seq_blocks(d, A.layer, sid);
         obs0 = sb.next - A.n_obs;
       }
-      // E4M3: every warp's share of the stage's scales is in (and its MMAs were issued)
+      // E4M3: every warp's share of the stage's decode, scales included, is in
       if constexpr (FP8) mbar_wait(d, sm, sm.kready[s % C::NK], (s / C::NK) & 1);
       mbar_wait(d, sm, sm.done[buf], (s >> 1) & 1);
       umma::fence_after();
