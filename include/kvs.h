@@ -318,8 +318,10 @@ KVS_API kvs_status kvs_decode_attend_static_scratch(kvs_ctx* ctx, int32_t layer,
  * caches convert the bf16 queries to f16 (exact in f16's normal range), as the
  * decode attend does.
  * Needs a context created with obs_window >= n_obs (tensor-core configurations
- * only).  Errors: KVS_ERR_INVALID_ARGUMENT for n_obs outside [1, obs_window], a
- * sequence holding fewer than n_obs entries, or (window mode) n_obs > window. */
+ * only).  One cooperative kernel launch (a CTA per SM) per 512 sequences of the call:
+ * a larger call runs as several launches, in order on the stream.  Errors:
+ * KVS_ERR_INVALID_ARGUMENT for n_obs outside [1, obs_window], a sequence holding fewer
+ * than n_obs entries, or (window mode) n_obs > window. */
 KVS_API kvs_status kvs_prefill_score(kvs_ctx* ctx, int32_t layer, kvs_seqs seqs, const void* d_q_obs,
                                      int32_t n_obs, kvs_stream_t stream);
 
