@@ -4,7 +4,8 @@ It compiles device-side bounds checks into the kernels for the indices the host 
 check (sequence ids read from a device list, pages, block ids), and fills the
 workspace regions that must be written before they are read with NaN.  A child
 process (the library is loaded once per process) runs a small case through the fused
-and the separate calls against the oracle with that build, then hands the kernels a
+and the separate calls and through SnapKV prefill scoring against the oracle with that
+build, then hands the kernels a
 device list whose ids disagree with the host list: the bounds checks must record
 KVS_ERR_STATE instead of touching memory out of range, and the context must stay
 usable after kvs_clear_error.
@@ -45,6 +46,17 @@ for name, fused in (("e4m3-window", True), ("bf16", False), ("e4m3-h2o", True)):
         harness.check_masses(run)
         harness.check_scores(run)
         harness.check_selection(run, keep)
+    assert run.cache.get_status() == 0, run.cache.last_error()
+
+# SnapKV prefill scoring: its scratch (row partials, per-group sums) starts NaN-filled,
+# so a read of a slot the launch did not write shows up in the masses
+from tests.test_gpu_snapkv import RHO
+for name in ("e4m3-window", "bf16-hkv8"):
+    wl = dataclasses.replace(SMALL[name], steps=1)
+    run = harness.Run(wl, oracle_seqs=list(range(wl.batch)), kernel=kvs.KERNEL_TENSOR, obs_window=32)
+    run.prefill()
+    run.prefill_score(32, rel=RHO)
+    harness.check_scores(run, rel=RHO)
     assert run.cache.get_status() == 0, run.cache.last_error()
 
 # a device list that disagrees with the host list: id 9 of 3 sequences
