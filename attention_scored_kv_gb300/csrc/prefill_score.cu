@@ -15,8 +15,9 @@
 //
 // How (one cooperative launch per layer, one CTA per SM):
 //   * The launch's (sequence, KV head, resident block) triples are laid end to end,
-//     sequence-major, and CTA c takes the contiguous share [c T / G, (c + 1) T / G).  A
-//     share cuts into runs, one per (sequence, KV head) group it touches.  Each run sees
+//     sequence-major, each group led by a fixed charge for its per-run costs, and CTA c
+//     takes the contiguous share [c T / G, (c + 1) T / G) of that weighted order.  A share
+//     cuts into runs, one per (sequence, KV head) group whose blocks it touches.  Each run sees
 //     the group's 8 heads x 32 observation rows (256 rows), staged once per group by TMA,
 //     and its keys 128 (8 blocks) per stage.
 //   * Phase 1 (row statistics): D = Q K^T, two M-128 halves of rows by N 128 keys, into
@@ -70,6 +71,10 @@ constexpr int kPool = 3;                               // max-pool radius (kerne
 constexpr int kInfo = 8;                               // stage-info ring
 constexpr int kScRing = 4;                             // E4M3 key-scale ring
 constexpr int kPieceList = 64;                         // pieces whose tickets wait for the end
+// A run costs about this many blocks on top of its blocks (the group's query copy, the
+// halo, the pool and the wait for the group's statistics), so the shares are cut in a
+// flattened order where each group carries kRunCost blocks before its own.
+constexpr int kRunCost = 12;
 static_assert(2 * kPieceList * kPieceMax <= kGq * kVoteKeys, "the winner list lives in the votes buffer");
 // An mbarrier poll suspends the thread until the phase completes or kSuspendNs pass, so
 // a waiting warp takes no issue slots; kMbarLimit polls (about a second) bound a wait.
@@ -112,7 +117,7 @@ struct PsShared {
   float merge[2][2][128];                              // phase 1: (max, sum) of the second key half
   int32_t pblk[kPieceMax + 2];                         // block ids of the piece's streamed blocks
   int32_t piece[kPieceList][3];                        // (group, first own block, end)
-  int32_t seq_off[kPsSeqMax + 1];                      // resident blocks before each sequence
+  int32_t seq_off[kPsSeqMax + 1];                      // weighted blocks before each sequence
 };
 
 struct PsArgs {
@@ -264,7 +269,7 @@ __device__ __forceinline__ RowWin row_window(const SeqBlocks& sb, int64_t p0, in
 struct Stage {
   int phase;            // 0: row statistics, 1: votes
   int sl, kvh, n;       // group (launch slot, KV head) and the sequence's resident blocks
-  int64_t gs;           // flattened index of the group's first block
+  int64_t gs;           // weighted flattened index of the group's first block
   int b0, nb;           // streamed blocks [b0, b0 + nb), group-local
   int v0, c0, c1;       // the piece's first streamed block and its own blocks [c0, c1)
   bool run_first, run_last, piece_last, new_q;
@@ -285,12 +290,13 @@ struct Sched {
     x1 = x1_;
     phase = 0;
     prev_g = -1;
-    live = x0 < x1;
-    if (live) start_run(x0);
+    live = x0 < x1 && start_run(x0);
   }
-  // the run holding flattened block x: its sequence is the last slot whose first block
-  // is at or before x (empty sequences hold no block, so the last such slot is not empty)
-  __device__ void start_run(int64_t x) {
+  // the first run at or after weighted index x, false if the share holds no block there.
+  // x's sequence is the last slot that starts at or before x (an empty sequence carries
+  // no weight, so that slot is not empty); x lies in a group's charge or in its blocks,
+  // and when the share ends inside the charge, no later group meets the share either.
+  __device__ bool start_run(int64_t x) {
     int lo = 0, hi = n_seqs - 1;
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
@@ -298,14 +304,17 @@ struct Sched {
       else hi = mid - 1;
     }
     sl = lo;
-    n = off[sl + 1] - off[sl];
+    const int w = off[sl + 1] - off[sl];
+    n = w - kRunCost;
     const int64_t base = (int64_t)hkv * off[sl];
-    kvh = (int)((x - base) / n);
-    gs = base + (int64_t)kvh * n;
+    kvh = (int)((x - base) / w);
+    gs = base + (int64_t)kvh * w + kRunCost;
     i1 = (int)(x1 - gs < n ? x1 - gs : n);
-    p0 = (int)(x - gs);
+    p0 = (int)(x > gs ? x - gs : 0);
+    if (i1 <= p0) return false;
     first = true;
     start_piece();
+    return true;
   }
   __device__ void start_piece() {
     if (phase == 0) {
@@ -346,8 +355,7 @@ struct Sched {
       } else {
         s.run_last = true;
         const int64_t x = gs + i1;
-        if (x < x1) {
-          start_run(x);
+        if (x < x1 && start_run(x)) {
         } else if (phase == 0) {
           phase = 1;
           start_run(x0);
@@ -375,12 +383,13 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
   const Dev& d = A.d;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  // ---- the launch's layout: seq_off[i] = resident blocks of slots 0 .. i-1
+  // ---- the launch's layout: seq_off[i] = weighted blocks of slots 0 .. i-1 (a sequence
+  // with n > 0 resident blocks weighs n + kRunCost per KV head)
   for (int i = tid; i < A.n_seqs; i += C::THREADS) {
     const int s = A.sel.at(i);
     int n = 0;
     if (KVS_DCHECK(d, s >= 0 && s < d.max_seqs)) n = min(seq_blocks(d, A.layer, s).n, d.ps_bound);
-    sm.seq_off[i + 1] = n;
+    sm.seq_off[i + 1] = n > 0 ? n + kRunCost : 0;
   }
   __syncthreads();
   if (warp == 0) {
@@ -403,8 +412,9 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
   __syncthreads();
   const int64_t T = (int64_t)d.Hkv * sm.seq_off[A.n_seqs];
   if (T == 0) return;
-  // CTAs with work: at least 4 blocks each, so every share is non-empty
-  const int64_t Ge = min((int64_t)gridDim.x, (T + 3) / 4);
+  // CTAs with work: shares of at least kRunCost + 4, so every share holds a block (between
+  // two groups' charges lies at least one block)
+  const int64_t Ge = min((int64_t)gridDim.x, max((int64_t)1, T / (kRunCost + 4)));
   const int c = blockIdx.x;
   if (c >= Ge) return;
   const int64_t x0 = c * T / Ge, x1 = (c + 1) * T / Ge;
@@ -578,7 +588,7 @@ __global__ void __launch_bounds__(PC<FP8>::THREADS, 1)
       const int slot = r & 1;
       if (r >= 2) mbar_wait(d, sm, sm.mp_empty[slot], ((r >> 1) - 1) & 1);
       const int g = st.sl * d.Hkv + st.kvh;
-      // the CTAs whose shares meet the group: CTA of flattened block x = ((x + 1) Ge - 1) / T
+      // the CTAs whose shares meet the group's blocks: CTA of weighted index x = ((x + 1) Ge - 1) / T
       const int cf = (int)(((st.gs + 1) * Ge - 1) / T), cl = (int)(((st.gs + st.n) * Ge - 1) / T);
       const int need = cl - cf + 1;
       if (lane == 0 && !wait_at_least(&d.ps_ready[g], need, d.spin_limit)) set_error(d, kErrTimeout);
