@@ -267,7 +267,7 @@ __device__ __forceinline__ RowWin row_window(const SeqBlocks& sb, int64_t p0, in
 // then phase 2 over the same runs, each cut into pieces whose streamed blocks include one
 // halo block on each side.
 struct Stage {
-  int phase;            // 0: row statistics, 1: votes
+  int phase;            // 0: phase 1 (row statistics), 1: phase 2 (votes)
   int sl, kvh, n;       // group (launch slot, KV head) and the sequence's resident blocks
   int64_t gs;           // weighted flattened index of the group's first block
   int b0, nb;           // streamed blocks [b0, b0 + nb), group-local
