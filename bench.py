@@ -568,7 +568,10 @@ def run_cpu_baseline(wl, steps):
         o.select(0, wl.keep_k(n_res // 16 + 1))
     dt = (time.perf_counter() - t0) / steps          # one sequence, one step
     value = 1.0 / (dt * wl.batch)                     # full batch: batch x that
+    # the KV bytes the sampled step scans (every layer, n_res entries) over its time
+    kv_gbs = n_res * kv_bytes_per_entry(wl) * wl.num_layers / dt / 1e9
     return {"value": round(value, 5), "unit": "decode steps/s", "cores": cores, "kind": "oracle",
+            "kv_gbs_equivalent": round(kv_gbs, 4),
             "sample": "%d decode steps of 1 of %d sequences (%d layers, %d resident entries each, float64 numpy); "
                       "the batch step is extrapolated as %d x the per-sequence step" % (
                           steps, wl.batch, wl.num_layers, n_res, wl.batch)}
@@ -617,6 +620,7 @@ def run_reference(args, world, rank):
         "config": {"workload": wl.name, "batch": wl.batch, "layers": wl.num_layers, "window": wl.window,
                    "kv_format": wl.kv_format},
         "cpu_baseline": {"value": round(value, 5), "unit": "decode steps/s", "cores": cores, "kind": "oracle",
+                         "kv_gbs_equivalent": round(n_res * kv_bytes_per_entry(wl) / per_layer_seq / 1e9, 4),
                          "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "decode steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

@@ -61,5 +61,5 @@ def test_reference_arm_under_torchrun_rank0_only():
     assert len(lines) == 1, r.stdout                 # rank 0 alone prints
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["kv_gbs_equivalent"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0
